@@ -1,0 +1,141 @@
+/*
+ * CPU oracle for the row-major FP32 matrix product C[M x N] = A[M x K] . B[K x N].
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: only the test suite, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes is the plain definition of the product, written out:
+ *
+ *     C[i,j] = sum_{k=0}^{K-1} A[i,k] * B[k,j]          0 <= i < M, 0 <= j < N
+ *
+ * ("Micro Kernel 입문하기", §3 "K 루프": the GEMM formula the register
+ *  accumulators c_ij hold; "누산 개념을 Grid-Block-Warp-Thread 계층에 끼워넣기",
+ *  §2 (4): every thread's acc[i][j] is stored to C[(row)*ldc + col]).
+ *
+ * Two accumulation modes:
+ *
+ *   oracle_gemm_f64*      each fp32 input is widened to double; a product of two
+ *                         fp32 values is exact in double; the K products are
+ *                         summed in double with k ascending.  This is the parity
+ *                         reference for every GPU result.
+ *
+ *   oracle_gemm_f32_fma_seq
+ *                         acc = fmaf(A[i,k], B[k,j], acc) in fp32 with k
+ *                         ascending, which is what the single-thread 4x4 example
+ *                         of "Micro Kernel 입문하기" §2 does once nvcc contracts
+ *                         `c += a*b` into one fused multiply-add (its default).
+ *                         Used only to reproduce that page's printed output.
+ *
+ * Storage is row-major with leading dimensions (elements between rows): A[i,k]
+ * is A[i*lda + k], B[k,j] is B[k*ldb + j], C[i,j] is C[i*ldc + j].  Elements in
+ * the padding of a row (column index >= the logical width) are never read or
+ * written.
+ *
+ * The loops run i -> k -> j with a row of double accumulators, so every C[i,j]
+ * still receives its K terms one at a time in ascending k; rows are independent
+ * and are spread over OpenMP threads, which does not change any result.
+ *
+ * Return value: 0 on success, -1 on invalid arguments (negative sizes, a leading
+ * dimension below the logical width, a null pointer with a non-empty extent).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static int bad_args(int M, int N, int K, const float* A, int64_t lda,
+                    const float* B, int64_t ldb, const void* C, int64_t ldc)
+{
+    if (M < 0 || N < 0 || K < 0) return 1;
+    if (lda < (K > 0 ? K : 1) || ldb < (N > 0 ? N : 1) || ldc < (N > 0 ? N : 1)) return 1;
+    if (M > 0 && K > 0 && A == NULL) return 1;
+    if (K > 0 && N > 0 && B == NULL) return 1;
+    if (M > 0 && N > 0 && C == NULL) return 1;
+    return 0;
+}
+
+static void one_row_f64(int N, int K, const float* Arow, const float* B, int64_t ldb,
+                        double* crow)
+{
+    for (int j = 0; j < N; ++j) crow[j] = 0.0;
+    for (int k = 0; k < K; ++k) {
+        const double a = (double)Arow[k];
+        const float* brow = B + (int64_t)k * ldb;
+        for (int j = 0; j < N; ++j) crow[j] += a * (double)brow[j];
+    }
+}
+
+/* Full product in double.  C is M x N doubles with leading dimension ldc. */
+int oracle_gemm_f64(int M, int N, int K, const float* A, int64_t lda, const float* B,
+                    int64_t ldb, double* C, int64_t ldc, int nthreads)
+{
+    if (bad_args(M, N, K, A, lda, B, ldb, C, ldc)) return -1;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int i = 0; i < M; ++i)
+        one_row_f64(N, K, A + (int64_t)i * lda, B, ldb, C + (int64_t)i * ldc);
+    return 0;
+}
+
+/* Selected rows only: out[r*N + j] = C[rows[r], j].  For full-size checks where
+ * the whole product would take too long on the host. */
+int oracle_gemm_f64_rows(int M, int N, int K, const float* A, int64_t lda, const float* B,
+                         int64_t ldb, const int32_t* rows, int nrows, double* out,
+                         int nthreads)
+{
+    if (bad_args(M, N, K, A, lda, B, ldb, out, N > 0 ? N : 1)) return -1;
+    if (nrows < 0 || (nrows > 0 && rows == NULL)) return -1;
+    for (int r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return -1;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int r = 0; r < nrows; ++r)
+        one_row_f64(N, K, A + (int64_t)rows[r] * lda, B, ldb, out + (int64_t)r * N);
+    return 0;
+}
+
+/* Selected elements only: out[e] = C[ii[e], jj[e]]. */
+int oracle_gemm_f64_elems(int M, int N, int K, const float* A, int64_t lda, const float* B,
+                          int64_t ldb, const int32_t* ii, const int32_t* jj, int n,
+                          double* out)
+{
+    if (bad_args(M, N, K, A, lda, B, ldb, out, N > 0 ? N : 1)) return -1;
+    if (n < 0 || (n > 0 && (ii == NULL || jj == NULL))) return -1;
+    for (int e = 0; e < n; ++e) {
+        if (ii[e] < 0 || ii[e] >= M || jj[e] < 0 || jj[e] >= N) return -1;
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k)
+            acc += (double)A[(int64_t)ii[e] * lda + k] * (double)B[(int64_t)k * ldb + jj[e]];
+        out[e] = acc;
+    }
+    return 0;
+}
+
+/* fp32 accumulation, one fused multiply-add per term, k ascending. */
+int oracle_gemm_f32_fma_seq(int M, int N, int K, const float* A, int64_t lda,
+                            const float* B, int64_t ldb, float* C, int64_t ldc)
+{
+    if (bad_args(M, N, K, A, lda, B, ldb, C, ldc)) return -1;
+    for (int i = 0; i < M; ++i)
+        for (int j = 0; j < N; ++j) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k)
+                acc = fmaf(A[(int64_t)i * lda + k], B[(int64_t)k * ldb + j], acc);
+            C[(int64_t)i * ldc + j] = acc;
+        }
+    return 0;
+}
+
+/* Threads an OpenMP region would use here (for reporting the CPU baseline). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
