@@ -1,0 +1,375 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 FP32 SGEMM (C = A.B, row-major, beta = 0).
+
+Default: the M=N=K=4096 workload (A, B ~ N(0,1) from seed 3) on one GPU; one
+JSON line on stdout.  A step is one sgemm_run over the resident inputs.  L2 is
+flushed (a 256 MiB write) before every step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on a bounded sample
+  python bench.py --sweep                # one line per named workload
+
+With N > 1 (torchrun) every rank runs its own replica of the workload: the
+product has no exchange step, so there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+REPO = os.path.dirname(os.path.abspath(__file__))
+if REPO not in sys.path:
+    sys.path.insert(0, REPO)
+
+from dense_fp32_gemm_09_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "sgemm_4096"
+METRIC = "SGEMM TFLOP/s (2MNK/t) at M=N=K=4096 FP32; % of GB300 FP32 CUDA-core peak"
+FMA_PER_CLK_PER_SM = 128          # FP32 lanes per SM (4 SMSPs x 32)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def describe(w) -> str:
+    dist = "N(0,1)" if w.dist == "normal" else f"U[{w.lo:g},{w.hi:g})"
+    return f"{w.name}: M={w.M} N={w.N} K={w.K} fp32 row-major, A,B ~ {dist} seed {w.seed}"
+
+
+KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_internal.h", "sgemm_kernels_main.cu"]
+
+
+def kernel_sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(REPO, "dense_fp32_gemm_09_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when there is
+    none for this kernel and workload or the kernel sources changed since."""
+    try:
+        with open(os.path.join(REPO, "profiles", "traffic_per_launch.txt")) as f:
+            lines = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    except OSError:
+        return None
+    cur = kernel_sources_hash()
+    for fields in lines:
+        if len(fields) >= 5 and fields[0] == kernel and fields[1] == workload and fields[4] == cur:
+            return int(fields[2]) + int(fields[3])
+    return None
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(REPO, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; reading only)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, torch_index: int, period_s: float = 0.01):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self.error = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.handle = ctypes.c_void_p()
+            if not self._find_handle(torch_index):
+                raise OSError("no NVML handle for this CUDA device")
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+        except OSError as e:
+            self.nvml = None
+            self.error = str(e)
+
+    def _find_handle(self, torch_index: int) -> bool:
+        """NVML handle of the CUDA device torch calls `torch_index` (matched by UUID,
+        then PCI address, since NVML numbers every GPU of the node)."""
+        import torch
+        props = torch.cuda.get_device_properties(torch_index)
+        uuid = getattr(props, "uuid", None)
+        if uuid is not None:
+            key = ("GPU-" + str(uuid)).encode()
+            if self.nvml.nvmlDeviceGetHandleByUUID(key, ctypes.byref(self.handle)) == 0:
+                return True
+        if hasattr(props, "pci_bus_id"):
+            bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                        getattr(props, "pci_device_id", 0))
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(),
+                                                           ctypes.byref(self.handle)) == 0:
+                return True
+        return self.nvml.nvmlDeviceGetHandleByIndex_v2(torch_index,
+                                                       ctypes.byref(self.handle)) == 0
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(int(clk.value))
+            if self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle,
+                                                                ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self) -> dict:
+        if self.nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": f"NVML unavailable: {self.error}"}
+        reasons = [n for bit, n in self.REASONS.items() if self.reasons & bit]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the oracle on a bounded sample (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def oracle_rate(w, A, B, target_s: float = 12.0, max_rows: int | None = None):
+    """TFLOP/s of the fp64 oracle on whole rows of C, sized to about target_s."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    An, Bn = A.numpy(), B.numpy()
+    threads = oracle.default_threads()
+    rows = max(1, min(w.M, 16))
+    t0 = time.perf_counter()
+    oracle.gemm_f64_rows(An, Bn, np.arange(rows, dtype=np.int32), nthreads=threads)
+    dt = time.perf_counter() - t0
+    per_row = dt / rows
+    want = int(max(1, min(w.M if max_rows is None else max_rows,
+                          (target_s - dt) / max(per_row, 1e-9))))
+    idx = np.linspace(0, w.M - 1, want).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.gemm_f64_rows(An, Bn, idx, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * want * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{want} of {w.M} rows of C (all N={w.N} columns, K={w.K}), "
+                      f"fp64 accumulation, {dt:.2f} s wall on {threads} threads",
+            "seconds": dt}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    A, B = make_inputs(w)
+    rates = []
+    steps_t = []
+    per_step_s = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        r = oracle_rate(w, A, B, target_s=per_step_s)
+        if i >= args.warmup:
+            rates.append(r["value"])
+            steps_t.append(r["seconds"])
+    value = statistics.median(rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(steps_t), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K},
+            "cpu_baseline": {**{k: v for k, v in r.items() if k != "seconds"}, "value": value},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+def bench_gpu(args, w, dist_ctx):
+    import torch
+
+    import dense_fp32_gemm_09_gb300 as sg
+    from dense_fp32_gemm_09_gb300._abi import check
+
+    rank, world, local = dist_ctx
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = sg.load()
+    A, B = make_inputs(w)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.empty(w.M, w.N, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    run_args = (w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N, dC.data_ptr(), w.N, sh)
+    cfg = sg.sgemm_query_config(w.M, w.N, w.K, w.K, w.N, w.N, dA.data_ptr(), dB.data_ptr(),
+                                dC.data_ptr())
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        check(lib.sgemm_run(*run_args), "sgemm_run")
+    barrier()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n_launch0 = lib.sgemm_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            check(lib.sgemm_run(*run_args), "sgemm_run")
+            ends[i].record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    launches = lib.sgemm_launch_count() - n_launch0
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    med_ms = statistics.median(step_ms)
+    mean_ms = statistics.fmean(step_ms)
+    if world > 1:
+        import torch.distributed as tdist
+        t = torch.tensor([med_ms, mean_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        med_ms, mean_ms = (float(x) for x in t.tolist())
+
+    # end to end through the host-buffer entry point: pinned host in, pinned host out
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.empty(w.M, w.N).pin_memory()
+    e2e_args = (w.M, w.N, w.K, hA.data_ptr(), w.K, hB.data_ptr(), w.N, hC.data_ptr(), w.N,
+                dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), sh)
+    for _ in range(max(1, min(args.warmup, 3))):
+        check(lib.sgemm_run_host(*e2e_args), "sgemm_run_host")
+    barrier()
+    e2e_steps = max(3, min(args.steps, 10))
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        check(lib.sgemm_run_host(*e2e_args), "sgemm_run_host")
+    ee.record(stream)
+    barrier()
+    e2e_ms = es.elapsed_time(ee) / e2e_steps
+    if world > 1:
+        import torch.distributed as tdist
+        t = torch.tensor([e2e_ms], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    max_mhz = float(peaks.get("sm_max_mhz") or clocks.summary().get("sm_max_mhz") or 2070.0)
+    peak_tflops = sms * FMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    flops = float(w.flops)
+    value = world * flops / (med_ms * 1e-3) / 1e12
+    achieved = flops / (med_ms * 1e-3) / 1e12
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": med_ms,
+        "ms_per_step_mean": mean_ms, "wall_s_timed_region": t_wall,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
+                   "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "kernel": cfg["name"], "grid": cfg["grid"], "tiles": cfg["tiles"],
+                   "sk_tiles": cfg["sk_tiles"], "ctas_per_sm": cfg["ctas_per_sm"],
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops,
+                     "unit": "TFLOP/s", "frac": achieved / peak_tflops,
+                     "traffic": recorded_traffic(cfg["name"], w.name),
+                     "algorithmic_bytes": w.min_bytes,
+                     "peak_basis": f"{sms} SMs x {FMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 x "
+                                   f"{max_mhz:.0f} MHz (max SM clock)",
+                     "frac_at_measured_clock": (
+                         achieved / (sms * FMA_PER_CLK_PER_SM * 2 * clk["sm_mhz"] * 1e-6)
+                         if clk.get("sm_mhz") else None)},
+        "clocks": clk,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
+                "d2h_bytes_per_step": 4 * w.M * w.N},
+        "gpu_launches": int(launches),
+    }
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--sweep", action="store_true", help="one line per named workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+    ctx = (rank, world, local)
+    names = sorted(WORKLOADS, key=lambda n: WORKLOADS[n].flops) if args.sweep else [w.name]
+    for name in names:
+        line = bench_gpu(args, WORKLOADS[name], ctx)
+        if line is not None and rank == 0:
+            if not args.no_cpu_baseline and world == 1 and not args.sweep:
+                A, B = make_inputs(WORKLOADS[name])
+                cb = oracle_rate(WORKLOADS[name], A, B, target_s=12.0)
+                cb.pop("seconds", None)
+                line["cpu_baseline"] = cb
+            print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.barrier()
+        tdist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,131 @@
+"""GB300-native FP32 SGEMM: C = A . B, row-major, on the CUDA cores of sm_103a.
+
+Thin Python face of the C ABI in ``include/sgemm.h``.  PyTorch supplies device
+memory and streams; every step of the product runs in the library's kernels.
+The library is loaded on first use and its absence is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from ._abi import (SGEMM_ERR_INVALID_ARG, SGEMM_ERR_LAUNCH, SGEMM_ERR_UNSUPPORTED,  # noqa: F401
+                   SGEMM_ERR_WORKSPACE, SGEMM_OK, SgemmConfig, SgemmError, check, load)
+
+__all__ = ["sgemm", "sgemm_run", "sgemm_run_ws", "sgemm_run_with", "sgemm_run_host",
+           "sgemm_query_config", "sgemm_workspace_size", "kernel_table", "launch_count",
+           "SgemmError", "load"]
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ld(t, name: str) -> int:
+    """Leading dimension of a 2-D row-major tensor view (unit column stride)."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its columns")
+    return max(t.stride(0), t.shape[1], 1)
+
+
+def _check_operand(t, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def sgemm_run(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream=None) -> int:
+    """Raw call of ``sgemm_run`` with integer device addresses; returns the status."""
+    return load().sgemm_run(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc,
+                            _stream_handle(stream))
+
+
+def sgemm_run_ws(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, ws_ptr, ws_bytes,
+                 stream=None) -> int:
+    return load().sgemm_run_ws(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, ws_ptr, ws_bytes,
+                               _stream_handle(stream))
+
+
+def sgemm_run_with(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, kernel_id, schedule=0,
+                   stream=None) -> int:
+    return load().sgemm_run_with(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, kernel_id,
+                                 schedule, _stream_handle(stream))
+
+
+def sgemm_run_host(M, N, K, hA, lda, hB, ldb, hC, ldc, dA, dB, dC, stream=None) -> int:
+    return load().sgemm_run_host(M, N, K, hA, lda, hB, ldb, hC, ldc, dA, dB, dC,
+                                 _stream_handle(stream))
+
+
+def sgemm_workspace_size(M, N, K, lda, ldb, ldc, A_ptr=None, B_ptr=None, C_ptr=None) -> int:
+    out = ctypes.c_size_t(0)
+    check(load().sgemm_workspace_size(M, N, K, lda, ldb, ldc, A_ptr, B_ptr, C_ptr,
+                                      ctypes.byref(out)), "sgemm_workspace_size")
+    return int(out.value)
+
+
+def sgemm_query_config(M, N, K, lda=None, ldb=None, ldc=None, A_ptr=None, B_ptr=None,
+                       C_ptr=None) -> dict:
+    cfg = SgemmConfig()
+    check(load().sgemm_query_config(M, N, K, lda or K, ldb or N, ldc or N, A_ptr, B_ptr, C_ptr,
+                                    ctypes.byref(cfg)), "sgemm_query_config")
+    d = cfg.as_dict()
+    d["name"] = load().sgemm_kernel_name(cfg.kernel_id).decode()
+    return d
+
+
+def kernel_table() -> list[dict]:
+    lib = load()
+    out = []
+    for i in range(lib.sgemm_num_kernels()):
+        cfg = SgemmConfig()
+        check(lib.sgemm_kernel_info(i, ctypes.byref(cfg)), "sgemm_kernel_info")
+        d = cfg.as_dict()
+        d["name"] = lib.sgemm_kernel_name(i).decode()
+        out.append(d)
+    return out
+
+
+def launch_count() -> int:
+    return int(load().sgemm_launch_count())
+
+
+def sgemm(A, B, out=None, *, kernel_id: int | None = None, schedule: int = 0, stream=None):
+    """C = A @ B for float32 CUDA tensors (row-major views with unit column stride).
+
+    ``out`` may be a preallocated (M, N) float32 CUDA view; it is overwritten.
+    ``kernel_id``/``schedule`` force a tile-table entry (tests and tuning)."""
+    import torch
+    _check_operand(A, "A")
+    _check_operand(B, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    else:
+        _check_operand(out, "out")
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must be {(M, N)}, got {tuple(out.shape)}")
+    if M == 0 or N == 0:
+        return out
+    lda, ldb, ldc = _ld(A, "A"), _ld(B, "B"), _ld(out, "out")
+    args = (M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc)
+    with torch.cuda.device(A.device):
+        if kernel_id is None and schedule == 0:
+            st = sgemm_run(*args, stream=stream)
+            check(st, "sgemm_run")
+        else:
+            st = sgemm_run_with(*args, -1 if kernel_id is None else kernel_id, schedule,
+                                stream=stream)
+            check(st, "sgemm_run_with")
+    return out

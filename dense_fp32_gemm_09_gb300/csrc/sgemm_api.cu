@@ -1,0 +1,651 @@
+// Host side of the C ABI declared in include/sgemm.h: argument checks, the
+// tile table and its selection, the persistent / stream-K schedule, workspaces
+// and launches.  No torch type crosses this boundary.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "sgemm_internal.h"
+#include "sgemm_sched.cuh"
+
+namespace sgemm {
+
+const KernelEntry* ffma_entries_main(int* count);
+const KernelEntry* ffma_entries_small(int* count);
+const KernelEntry* ffma_entries_any(int* count);
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char t_last_error[512] = "";
+
+void set_error(const char* what, cudaError_t e) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "%s: %s (%s)", what,
+                  cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ----------------------------------------------------------------------------
+// Tile table
+// ----------------------------------------------------------------------------
+const std::vector<KernelEntry>& table() {
+    static const std::vector<KernelEntry> t = [] {
+        std::vector<KernelEntry> v;
+        int n = 0;
+        const KernelEntry* e = ffma_entries_main(&n);
+        v.insert(v.end(), e, e + n);
+        e = ffma_entries_small(&n);
+        v.insert(v.end(), e, e + n);
+        e = ffma_entries_any(&n);
+        v.insert(v.end(), e, e + n);
+        return v;
+    }();
+    return t;
+}
+
+int find_entry(const char* name) {
+    const auto& t = table();
+    for (size_t i = 0; i < t.size(); ++i)
+        if (std::strcmp(t[i].name, name) == 0) return static_cast<int>(i);
+    return -1;
+}
+
+// Per-device facts and per-(device, entry) residency, computed once.
+struct DeviceInfo {
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    std::vector<int> occ;  // resident CTAs per SM for each table entry (0 = unusable)
+};
+
+std::mutex g_dev_mu;
+std::map<int, DeviceInfo> g_dev;
+
+int device_info(int dev, const DeviceInfo** out) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    auto it = g_dev.find(dev);
+    if (it != g_dev.end()) {
+        *out = &it->second;
+        return SGEMM_OK;
+    }
+    DeviceInfo info;
+    cudaError_t e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) {
+        set_error("cudaDeviceGetAttribute", e);
+        return SGEMM_ERR_LAUNCH;
+    }
+    if (info.cc_major != 10 || info.cc_minor != 3) {
+        std::snprintf(t_last_error, sizeof(t_last_error),
+                      "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                      info.cc_major, info.cc_minor);
+        return SGEMM_ERR_UNSUPPORTED;
+    }
+    const auto& t = table();
+    info.occ.assign(t.size(), 0);
+    for (size_t i = 0; i < t.size(); ++i) {
+        e = cudaFuncSetAttribute(t[i].kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 t[i].smem_bytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(t[i].kernel,
+                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        int occ = 0;
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, t[i].kernel, t[i].threads,
+                                                              t[i].smem_bytes);
+        if (e != cudaSuccess) {
+            set_error("kernel attribute / occupancy query", e);
+            return SGEMM_ERR_LAUNCH;
+        }
+        info.occ[i] = occ;
+    }
+    auto res = g_dev.emplace(dev, std::move(info));
+    *out = &res.first->second;
+    return SGEMM_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Argument checks
+// ----------------------------------------------------------------------------
+bool ranges_overlap(const float* p, long long n, const float* q, long long m) {
+    if (n <= 0 || m <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + 4ull * n;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(q), b1 = b0 + 4ull * m;
+    return a0 < b1 && b0 < a1;
+}
+
+// Elements spanned by a rows x cols row-major matrix with leading dimension ld.
+long long span(int rows, int cols, int ld) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return static_cast<long long>(rows - 1) * ld + cols;
+}
+
+int check_args(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+               const float* C, int ldc) {
+    if (M < 0 || N < 0 || K < 0) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "negative size M=%d N=%d K=%d", M,
+                      N, K);
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    if (lda < std::max(K, 1) || ldb < std::max(N, 1) || ldc < std::max(N, 1)) {
+        std::snprintf(t_last_error, sizeof(t_last_error),
+                      "leading dimension below row width: lda=%d (K=%d) ldb=%d ldc=%d (N=%d)",
+                      lda, K, ldb, ldc, N);
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    if ((M > 0 && N > 0 && C == nullptr) || (M > 0 && N > 0 && K > 0 && (A == nullptr ||
+                                                                          B == nullptr))) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "null pointer with non-empty extent");
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    if (M > 0 && N > 0 && K > 0) {
+        const long long sc = span(M, N, ldc);
+        if (ranges_overlap(C, sc, A, span(M, K, lda)) ||
+            ranges_overlap(C, sc, B, span(K, N, ldb))) {
+            std::snprintf(t_last_error, sizeof(t_last_error), "C overlaps A or B");
+            return SGEMM_ERR_INVALID_ARG;
+        }
+    }
+    return SGEMM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ----------------------------------------------------------------------------
+// Selection and schedule
+// ----------------------------------------------------------------------------
+struct Plan {
+    int entry = -1;
+    GemmArgs args{};
+    size_t ws_partial_bytes = 0;  // bytes of partial tiles
+    int ctas_per_sm = 0;
+    int split = 1;
+    int sms = 0;
+};
+
+
+// 16-byte cp.async needs every A and B row to start on a 16-byte boundary.
+bool vec4_ok(const float* A, int lda, const float* B, int ldb) {
+    return aligned16(A) && aligned16(B) && (lda % 4 == 0) && (ldb % 4 == 0);
+}
+
+bool entry_fits(const KernelEntry& e, const float* A, int lda, const float* B, int ldb) {
+    return e.vec != 4 || vec4_ok(A, lda, B, ldb);
+}
+
+int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int lda,
+                 const float* B, int ldb) {
+    if (const char* force = std::getenv("SGEMM_FORCE_KERNEL")) {
+        const int id = find_entry(force);
+        if (id >= 0 && entry_fits(table()[id], A, lda, B, ldb) && d.occ[id] > 0)
+            return id;
+    }
+    const bool v4 = vec4_ok(A, lda, B, ldb);
+    const long long tiles128 = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
+    const char* name;
+    if (v4 && N <= 64)
+        name = "128x64x16_t16x8_s4_f2_v4";
+    else if (tiles128 * 4 < d.sms)
+        name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
+    else if (v4)
+        name = K >= 2048 ? "128x256x64_t8x16_s2_f2_v4" : "128x256x32_t8x16_s4_f2_v4";
+    else
+        name = "128x256x32_t8x16_s3_f2_v1";
+    return find_entry(name);
+}
+
+// schedule: 0 automatic, 1 data-parallel only, 2 stream-K whenever possible.
+void make_schedule(int sms, int occ, int entry, int schedule, Plan& p) {
+    const KernelEntry& e = table()[entry];
+    const SchedSizes z = plan_schedule(p.args, e.bm, e.bn, e.bk, sms, occ, schedule);
+    p.ctas_per_sm = occ;
+    p.split = z.split;
+    p.ws_partial_bytes = z.partial_bytes;
+}
+
+int plan(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+         int ldc, int forced_entry, int schedule, Plan& p, const DeviceInfo** dinfo) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error("cudaGetDevice", e);
+        return SGEMM_ERR_UNSUPPORTED;
+    }
+    const DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != SGEMM_OK) return rc;
+    *dinfo = d;
+    const auto& t = table();
+    int entry = forced_entry;
+    if (entry >= 0) {
+        if (entry >= static_cast<int>(t.size()) || !entry_fits(t[entry], A, lda, B, ldb) ||
+            d->occ[entry] <= 0) {
+            std::snprintf(t_last_error, sizeof(t_last_error),
+                          "kernel %d cannot serve these operands", entry);
+            return SGEMM_ERR_UNSUPPORTED;
+        }
+    } else {
+        entry = choose_entry(*d, M, N, K, A, lda, B, ldb);
+        if (entry < 0) {
+            std::snprintf(t_last_error, sizeof(t_last_error), "no tile-table entry");
+            return SGEMM_ERR_UNSUPPORTED;
+        }
+    }
+    p.entry = entry;
+    GemmArgs& a = p.args;
+    a.M = M; a.N = N; a.K = K;
+    a.A = A; a.B = B; a.C = C;
+    a.lda = lda; a.ldb = ldb; a.ldc = ldc;
+    a.c_vec = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    make_schedule(d->sms, d->occ[entry], entry, schedule, p);
+    return SGEMM_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Workspaces owned by the library: one per (device, stream), grown on demand
+// with the stream-ordered allocator so a resize never races in-flight work.
+// ----------------------------------------------------------------------------
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+int library_workspace(cudaStream_t stream, size_t need, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error("cudaGetDevice", e);
+        return SGEMM_ERR_LAUNCH;
+    }
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Workspace& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (w.bytes >= need) {
+        *out = w.ptr;
+        return SGEMM_OK;
+    }
+    if (w.ptr) {
+        e = cudaFreeAsync(w.ptr, stream);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (e != cudaSuccess) {
+            set_error("cudaFreeAsync", e);
+            return SGEMM_ERR_WORKSPACE;
+        }
+    }
+    const size_t bytes = std::max(need, static_cast<size_t>(1) << 20);
+    e = cudaMallocAsync(&w.ptr, bytes, stream);
+    if (e != cudaSuccess) {
+        w.ptr = nullptr;
+        set_error("cudaMallocAsync", e);
+        return SGEMM_ERR_WORKSPACE;
+    }
+    w.bytes = bytes;
+    *out = w.ptr;
+    return SGEMM_OK;
+}
+
+__global__ void zero_fill_kernel(float* C, int M, int N, long long ldc) {
+    const long long total = static_cast<long long>(M) * N;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long i = e / N, j = e - i * N;
+        C[i * ldc + j] = 0.0f;
+    }
+}
+
+int launch_zero(float* C, int M, int N, int ldc, cudaStream_t stream, const DeviceInfo* d) {
+    const long long total = static_cast<long long>(M) * N;
+    const int threads = 256;
+    const long long blocks =
+        std::min<long long>((total + threads - 1) / threads, static_cast<long long>(d->sms) * 8);
+    zero_fill_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(C, M, N, ldc);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("zero_fill_kernel launch", e);
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
+}
+
+int launch(const Plan& p, cudaStream_t stream) {
+    const KernelEntry& e = table()[p.entry];
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.args.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(e.threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(e.smem_bytes);
+    cfg.stream = stream;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    GemmArgs args = p.args;
+    void* params[] = {&args};
+    cudaError_t err = cudaLaunchKernelExC(&cfg, e.kernel, params);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (err == cudaSuccess) err = cudaGetLastError();
+    if (err != cudaSuccess) {
+        set_error(e.name, err);
+        return SGEMM_ERR_LAUNCH;
+    }
+    if (p.args.sk_tiles > 0) {
+        err = launch_sk_reduce(p.args, e.bm, e.bn, p.sms, stream);
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        if (err != cudaSuccess) {
+            set_error("sk_reduce_kernel", err);
+            return SGEMM_ERR_LAUNCH;
+        }
+    }
+    return SGEMM_OK;
+}
+
+// Common body of the run entry points.  ws == nullptr with ws_bytes == SIZE_MAX
+// means "use the library-owned workspace".
+int run_impl(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+             int ldc, int forced_entry, int schedule, void* ws, size_t ws_bytes,
+             bool library_ws, cudaStream_t stream) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    Plan p;
+    const DeviceInfo* d = nullptr;
+    if (K == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) {
+            set_error("cudaGetDevice", e);
+            return SGEMM_ERR_UNSUPPORTED;
+        }
+        rc = device_info(dev, &d);
+        if (rc != SGEMM_OK) return rc;
+        return launch_zero(C, M, N, ldc, stream, d);
+    }
+    rc = plan(M, N, K, A, lda, B, ldb, C, ldc, forced_entry, schedule, p, &d);
+    if (rc != SGEMM_OK) return rc;
+    const size_t need = p.ws_partial_bytes;
+    if (need > 0) {
+        void* base = nullptr;
+        if (library_ws) {
+            rc = library_workspace(stream, need, &base);
+            if (rc != SGEMM_OK) return rc;
+        } else {
+            if (ws == nullptr || ws_bytes < need || !aligned16(ws)) {
+                std::snprintf(t_last_error, sizeof(t_last_error),
+                              "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+                return SGEMM_ERR_WORKSPACE;
+            }
+            base = ws;
+        }
+        p.args.ws_partial = static_cast<float*>(base);
+    }
+    p.sms = d->sms;
+    return launch(p, stream);
+}
+
+void fill_config(const Plan& p, sgemm_config* out) {
+    const KernelEntry& e = table()[p.entry];
+    out->bm = e.bm; out->bn = e.bn; out->bk = e.bk;
+    out->wm = e.wm; out->wn = e.wn; out->tm = e.tm; out->tn = e.tn;
+    out->stages = e.stages; out->threads = e.threads; out->smem_bytes = e.smem_bytes;
+    out->split_k = p.split;
+    out->kernel_id = p.entry;
+    out->vec = e.vec;
+    out->grid = p.args.grid;
+    out->tiles = p.args.tiles_m * p.args.tiles_n;
+    out->sk_tiles = p.args.sk_tiles;
+    out->ctas_per_sm = p.ctas_per_sm;
+    out->fma2 = e.fma2;
+}
+
+// Walks every CTA's flat slice list exactly as the kernel does and checks the
+// schedule: each (tile, k-slice) is computed once, tile origins are distinct and
+// inside C, every split tile's contributors write slots 0/1 only and number
+// exactly what the kernel's owner formula expects.
+int check_schedule(const Plan& p, char* why, size_t why_len) {
+    const KernelEntry& e = table()[p.entry];
+    const GemmArgs& a = p.args;
+    const long long T = static_cast<long long>(a.tiles_m) * a.tiles_n;
+    const int KT = a.KT, G = a.grid;
+    auto fail = [&](const char* msg, long long x, long long y) {
+        std::snprintf(why, why_len, "%s (%lld, %lld)", msg, x, y);
+        return SGEMM_ERR_INVALID_ARG;
+    };
+    if (G <= 0 || a.dp_tiles + a.sk_tiles != T) return fail("tile count", G, T);
+    if (a.sk_tiles > 0 && a.sk_iters < G) return fail("stream-K range empty", a.sk_iters, G);
+    if (a.sk_tiles > G) return fail("more split tiles than CTAs", a.sk_tiles, G);
+    std::vector<unsigned char> cover(static_cast<size_t>(T) * KT, 0);
+    std::vector<int> contrib(static_cast<size_t>(a.sk_tiles), 0);
+    for (int g = 0; g < G; ++g) {
+        const CtaWork w = make_work(a, g);
+        if (w.total <= 0) return fail("CTA without work", g, w.total);
+        Cursor c;
+        c.seek(w, 0);
+        for (long long it = 0; it < w.total; ++it) {
+            if (c.tile < 0 || c.tile >= T || c.kt < 0 || c.kt >= KT || c.kt < c.kt_begin ||
+                c.kt >= c.kt_end)
+                return fail("cursor out of range", c.tile, c.kt);
+            if (++cover[static_cast<size_t>(c.tile) * KT + c.kt] != 1)
+                return fail("slice computed twice", c.tile, c.kt);
+            if (c.kt + 1 == c.kt_end && !(c.kt_begin == 0 && c.kt_end == KT)) {
+                const int t = c.tile - a.dp_tiles;
+                if (t < 0 || t >= a.sk_tiles) return fail("partial outside split tiles", g, t);
+                const int slot = sk_slot(w, t);
+                if (slot < 0 || slot > 1) return fail("slot out of range", g, slot);
+                ++contrib[static_cast<size_t>(t)];
+            }
+            c.advance(w);
+        }
+    }
+    for (size_t i = 0; i < cover.size(); ++i)
+        if (cover[i] != 1) return fail("slice never computed", static_cast<long long>(i / KT),
+                                       static_cast<long long>(i % KT));
+    for (int t = 0; t < a.sk_tiles; ++t) {
+        const long long tb = static_cast<long long>(t) * KT;
+        const int g0 = sk_owner(tb, G, a.sk_iters), g1 = sk_owner(tb + KT - 1, G, a.sk_iters);
+        if (contrib[t] == 0) {
+            if (g0 != g1) return fail("whole split tile with several owners", t, g1 - g0);
+            continue;
+        }
+        if (contrib[t] != g1 - g0 + 1) return fail("contributor count", t, contrib[t]);
+        if (contrib[t] > kMaxSplit) return fail("too many contributors", t, contrib[t]);
+        for (int gg = g0; gg <= g1; ++gg) {
+            const int sl = t - static_cast<int>((a.sk_iters * gg / G) / KT);
+            if (sl < 0 || sl > 1) return fail("reduction slot out of range", t, gg);
+        }
+    }
+    std::vector<unsigned char> seen(static_cast<size_t>(T), 0);
+    for (long long tile = 0; tile < T; ++tile) {
+        int m0 = 0, n0 = 0;
+        tile_origin(a, static_cast<int>(tile), e.bm, e.bn, m0, n0);
+        if (m0 < 0 || n0 < 0 || m0 >= a.M || n0 >= a.N || m0 % e.bm || n0 % e.bn)
+            return fail("tile origin outside C", m0, n0);
+        const size_t id = static_cast<size_t>(m0 / e.bm) * a.tiles_n + n0 / e.bn;
+        if (seen[id]++) return fail("tile origin repeated", m0, n0);
+    }
+    return SGEMM_OK;
+}
+
+}  // namespace
+}  // namespace sgemm
+
+using namespace sgemm;
+
+extern "C" {
+
+int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
+              int ldc, sgemm_stream_t stream) {
+    return run_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, 0, nullptr, 0, true,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                 float* C, int ldc, void* ws, size_t ws_bytes, sgemm_stream_t stream) {
+    return run_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, 0, ws, ws_bytes, false,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_run_with(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                   float* C, int ldc, int kernel_id, int schedule, sgemm_stream_t stream) {
+    if (kernel_id < -1 || schedule < 0 || schedule > 2) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "bad kernel_id %d or schedule %d",
+                      kernel_id, schedule);
+        return kernel_id < -1 ? SGEMM_ERR_UNSUPPORTED : SGEMM_ERR_INVALID_ARG;
+    }
+    return run_impl(M, N, K, A, lda, B, ldb, C, ldc, kernel_id, schedule, nullptr, 0, true,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_workspace_size(int M, int N, int K, int lda, int ldb, int ldc, const float* A,
+                         const float* B, const float* C, size_t* out_bytes) {
+    if (out_bytes == nullptr) return SGEMM_ERR_INVALID_ARG;
+    *out_bytes = 0;
+    // Alignment-only use of the pointers: substitute aligned stand-ins for NULL.
+    const float* pa = A ? A : reinterpret_cast<const float*>(uintptr_t{256});
+    const float* pb = B ? B : reinterpret_cast<const float*>(uintptr_t{256} << 20);
+    const float* pc = C ? C : reinterpret_cast<const float*>(uintptr_t{256} << 40);
+    if (M < 0 || N < 0 || K < 0 || lda < std::max(K, 1) || ldb < std::max(N, 1) ||
+        ldc < std::max(N, 1))
+        return SGEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0 || K == 0) return SGEMM_OK;
+    Plan p;
+    const DeviceInfo* d = nullptr;
+    const int rc = plan(M, N, K, pa, lda, pb, ldb, const_cast<float*>(pc), ldc, -1, 0, p, &d);
+    if (rc != SGEMM_OK) return rc;
+    *out_bytes = p.ws_partial_bytes;
+    return SGEMM_OK;
+}
+
+int sgemm_query_config(int M, int N, int K, int lda, int ldb, int ldc, const float* A,
+                       const float* B, const float* C, sgemm_config* out) {
+    if (out == nullptr) return SGEMM_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof(*out));
+    const float* pa = A ? A : reinterpret_cast<const float*>(uintptr_t{256});
+    const float* pb = B ? B : reinterpret_cast<const float*>(uintptr_t{256} << 20);
+    const float* pc = C ? C : reinterpret_cast<const float*>(uintptr_t{256} << 40);
+    if (M <= 0 || N <= 0 || K <= 0 || lda < K || ldb < N || ldc < N)
+        return SGEMM_ERR_INVALID_ARG;
+    Plan p;
+    const DeviceInfo* d = nullptr;
+    const int rc = plan(M, N, K, pa, lda, pb, ldb, const_cast<float*>(pc), ldc, -1, 0, p, &d);
+    if (rc != SGEMM_OK) return rc;
+    fill_config(p, out);
+    return SGEMM_OK;
+}
+
+int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* hB, int ldb,
+                   float* hC, int ldc, float* dA, float* dB, float* dC, sgemm_stream_t stream) {
+    int rc = check_args(M, N, K, hA, lda, hB, ldb, hC, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (dC == nullptr || (K > 0 && (dA == nullptr || dB == nullptr))) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "null device buffer");
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (K > 0) {
+        e = cudaMemcpy2DAsync(dA, sizeof(float) * lda, hA, sizeof(float) * lda,
+                              sizeof(float) * K, M, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(dB, sizeof(float) * ldb, hB, sizeof(float) * ldb,
+                                  sizeof(float) * N, K, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) {
+            set_error("host-to-device copy", e);
+            return SGEMM_ERR_LAUNCH;
+        }
+    }
+    rc = sgemm_run(M, N, K, dA, lda, dB, ldb, dC, ldc, stream);
+    if (rc != SGEMM_OK) return rc;
+    e = cudaMemcpy2DAsync(hC, sizeof(float) * ldc, dC, sizeof(float) * ldc, sizeof(float) * N,
+                          M, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) {
+        set_error("device-to-host copy", e);
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
+}
+
+int sgemm_schedule_check(int M, int N, int K, int kernel_id, int sms, int ctas_per_sm,
+                         int schedule, sgemm_config* out) {
+    if (M <= 0 || N <= 0 || K <= 0 || sms <= 0 || ctas_per_sm <= 0 || schedule < 0 ||
+        schedule > 2 || kernel_id < 0 || kernel_id >= static_cast<int>(table().size()))
+        return SGEMM_ERR_INVALID_ARG;
+    Plan p;
+    p.entry = kernel_id;
+    p.args.M = M; p.args.N = N; p.args.K = K;
+    make_schedule(sms, ctas_per_sm, kernel_id, schedule, p);
+    if (out) fill_config(p, out);
+    return check_schedule(p, t_last_error, sizeof(t_last_error));
+}
+
+int sgemm_num_kernels(void) { return static_cast<int>(table().size()); }
+
+int sgemm_kernel_info(int kernel_id, sgemm_config* out) {
+    if (out == nullptr) return SGEMM_ERR_INVALID_ARG;
+    if (kernel_id < 0 || kernel_id >= static_cast<int>(table().size()))
+        return SGEMM_ERR_UNSUPPORTED;
+    std::memset(out, 0, sizeof(*out));
+    const KernelEntry& e = table()[kernel_id];
+    out->bm = e.bm; out->bn = e.bn; out->bk = e.bk;
+    out->wm = e.wm; out->wn = e.wn; out->tm = e.tm; out->tn = e.tn;
+    out->stages = e.stages; out->threads = e.threads; out->smem_bytes = e.smem_bytes;
+    out->kernel_id = kernel_id;
+    out->vec = e.vec;
+    out->fma2 = e.fma2;
+    return SGEMM_OK;
+}
+
+const char* sgemm_kernel_name(int kernel_id) {
+    if (kernel_id < 0 || kernel_id >= static_cast<int>(table().size())) return "";
+    return table()[kernel_id].name;
+}
+
+const char* sgemm_status_string(int status) {
+    switch (status) {
+        case SGEMM_OK: return "SGEMM_OK";
+        case SGEMM_ERR_INVALID_ARG: return "SGEMM_ERR_INVALID_ARG";
+        case SGEMM_ERR_ALIGNMENT: return "SGEMM_ERR_ALIGNMENT";
+        case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH";
+        case SGEMM_ERR_UNSUPPORTED: return "SGEMM_ERR_UNSUPPORTED";
+        case SGEMM_ERR_TIMEOUT: return "SGEMM_ERR_TIMEOUT";
+        case SGEMM_ERR_WORKSPACE: return "SGEMM_ERR_WORKSPACE";
+        default: return "SGEMM_ERR_UNKNOWN";
+    }
+}
+
+const char* sgemm_last_error(void) { return t_last_error; }
+
+uint64_t sgemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int sgemm_shutdown(void) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    int rc = SGEMM_OK;
+    for (auto& kv : g_ws) {
+        if (kv.second.ptr) {
+            int prev = 0;
+            cudaGetDevice(&prev);
+            cudaSetDevice(kv.first.first);
+            const cudaError_t e = cudaFree(kv.second.ptr);
+            cudaSetDevice(prev);
+            if (e != cudaSuccess) {
+                set_error("cudaFree", e);
+                rc = SGEMM_ERR_LAUNCH;
+            }
+        }
+    }
+    g_ws.clear();
+    return rc;
+}
+
+}  // extern "C"

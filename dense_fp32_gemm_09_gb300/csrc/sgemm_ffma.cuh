@@ -1,0 +1,421 @@
+// FP32 SGEMM on the CUDA cores of sm_103a: persistent, multistage cp.async
+// pipeline, register outer-product micro-kernel, stream-K tail balancing.
+//
+// The hierarchy is the one the source pages describe ("누산 개념을
+// Grid-Block-Warp-Thread 계층에 끼워넣기", §2 (1)-(4); "Register/Shared Memory
+// Tiling", 동작 원리 and 아웃터 프로덕트 GEMM):
+//   * a CTA computes BM x BN tiles of C,
+//   * a warp owns a WM x WN warp tile inside the CTA tile,
+//   * a thread owns a TM x TN register tile acc[TM][TN],
+//   * the K range is walked in BK-deep slices staged in shared memory, and
+//     every k of a slice applies the rank-1 update acc[i][j] += a[i] * b[j]
+//     ("기존 작성한 GE_v2 의 regemm 타일드 커널의 1:1 매핑, gemm_tiled_test 작성",
+//     §5: one fmaf per accumulator per k).
+//
+// What is different from the pages' kernels, and why (GB300 first):
+//   * Loads are cp.async (16-byte .cg when rows are 16-byte aligned, 4-byte .ca
+//     otherwise) into a STAGES-deep ring of shared-memory slices instead of the
+//     pages' synchronous single / double buffer ("Register/Shared Memory
+//     Tiling", 더블 버퍼링 구현), so global latency overlaps several slices of math.
+//   * Out-of-range elements are zero-filled by the copy itself (src-size 0 or a
+//     short src-size), which is the pages' "boundary check then 0-padding"
+//     (GE_v2 page, §3) without a branch around the copy.
+//   * The A slice keeps its global row-major layout with a 4-float row pad; a
+//     thread reads AK consecutive k of one row per LDS, and the odd row stride
+//     in 16-byte units puts the LR rows a warp reads in distinct banks.  The B
+//     slice is unpadded; each LDS.128 of a warp touches LC consecutive 16-byte
+//     chunks of one row.  (The pages' `+PADK/+PADN` padding, GE_v2 page §2.)
+//   * The grid is persistent (SM count x resident CTAs).  Each CTA walks a flat
+//     list of k-slices that may cross tile boundaries, so the copy pipeline
+//     never drains between tiles.  Whole waves of tiles are data-parallel; the
+//     last partial wave is shared out by k-slices over all CTAs (stream-K).  Each
+//     CTA writes its partial tiles to a workspace and a second, bandwidth-bound
+//     kernel (sgemm_reduce.cuh) sums every split tile's partials over all SMs in
+//     a fixed order, so results are identical from run to run.
+#pragma once
+
+#include <stdint.h>
+
+#include "sgemm_internal.h"
+#include "sgemm_sched.cuh"
+
+namespace sgemm {
+
+// ----------------------------------------------------------------------------
+// PTX helpers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const float* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+                 "l"(__cvta_generic_to_global(src)), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float* src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst),
+                 "l"(__cvta_generic_to_global(src)), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Packed pair of fp32 accumulators: low 32 bits = column j, high = column j+1.
+__device__ __forceinline__ void ffma2_bcast(unsigned long long& d, float a,
+                                            unsigned long long b) {
+    asm("{\n\t.reg .b64 ta;\n\t"
+        "mov.b64 ta, {%1, %1};\n\t"
+        "fma.rn.f32x2 %0, ta, %2, %0;\n\t}"
+        : "+l"(d)
+        : "f"(a), "l"(b));
+}
+
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float lo_f(unsigned long long x) {
+    return __uint_as_float(static_cast<uint32_t>(x));
+}
+__device__ __forceinline__ float hi_f(unsigned long long x) {
+    return __uint_as_float(static_cast<uint32_t>(x >> 32));
+}
+
+// ----------------------------------------------------------------------------
+// Register accumulators: plain fp32, or packed pairs for fma.rn.f32x2
+// ----------------------------------------------------------------------------
+template <int TM, int TN, bool FMA2>
+struct Acc;
+
+template <int TM, int TN>
+struct Acc<TM, TN, false> {
+    float v[TM][TN];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) v[i][j] = 0.0f;
+    }
+    // b holds TN values of one k (TN/4 float4 chunks).
+    __device__ __forceinline__ void rank1(const float (&a)[TM], const float4 (&b)[TN / 4]) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j4 = 0; j4 < TN / 4; ++j4) {
+                v[i][4 * j4 + 0] = fmaf(a[i], b[j4].x, v[i][4 * j4 + 0]);
+                v[i][4 * j4 + 1] = fmaf(a[i], b[j4].y, v[i][4 * j4 + 1]);
+                v[i][4 * j4 + 2] = fmaf(a[i], b[j4].z, v[i][4 * j4 + 2]);
+                v[i][4 * j4 + 3] = fmaf(a[i], b[j4].w, v[i][4 * j4 + 3]);
+            }
+    }
+    __device__ __forceinline__ float4 chunk(int i, int j4) const {
+        return make_float4(v[i][4 * j4], v[i][4 * j4 + 1], v[i][4 * j4 + 2], v[i][4 * j4 + 3]);
+    }
+};
+
+template <int TM, int TN>
+struct Acc<TM, TN, true> {
+    unsigned long long v[TM][TN / 2];
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN / 2; ++j) v[i][j] = 0ull;
+    }
+    __device__ __forceinline__ void rank1(const float (&a)[TM], const float4 (&b)[TN / 4]) {
+        unsigned long long bp[TN / 2];
+#pragma unroll
+        for (int j4 = 0; j4 < TN / 4; ++j4) {
+            bp[2 * j4] = pack2(b[j4].x, b[j4].y);
+            bp[2 * j4 + 1] = pack2(b[j4].z, b[j4].w);
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN / 2; ++j) ffma2_bcast(v[i][j], a[i], bp[j]);
+    }
+    __device__ __forceinline__ float4 chunk(int i, int j4) const {
+        return make_float4(lo_f(v[i][2 * j4]), hi_f(v[i][2 * j4]), lo_f(v[i][2 * j4 + 1]),
+                           hi_f(v[i][2 * j4 + 1]));
+    }
+};
+
+// ----------------------------------------------------------------------------
+// The kernel
+// ----------------------------------------------------------------------------
+template <int BM_, int BN_, int BK_, int TM_, int TN_, int LR_, int WARPS_M_, int WARPS_N_,
+          int STAGES_, int VEC_, int AK_, bool FMA2_, int MINB_>
+struct FfmaCfg {
+    static constexpr int BM = BM_, BN = BN_, BK = BK_, TM = TM_, TN = TN_;
+    static constexpr int LR = LR_, LC = 32 / LR_;
+    static constexpr int WM = TM * LR, WN = TN * LC;
+    static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
+    static constexpr int NT = 32 * WARPS_M * WARPS_N;
+    static constexpr int STAGES = STAGES_, VEC = VEC_, AK = AK_;
+    static constexpr bool FMA2 = FMA2_;
+    static constexpr int MINB = MINB_;
+    // A slice: [BM][BK + PADA] (row stride odd in 16-byte units); B slice: [BK][BN].
+    static constexpr int PADA = ((BK / 4) % 2 == 0) ? 4 : 0;
+    static constexpr int LDAS = BK + PADA;
+    static constexpr int LDBS = BN;
+    static constexpr int A_STAGE = BM * LDAS;
+    static constexpr int B_STAGE = BK * LDBS;
+    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+
+    static_assert(BM == WM * WARPS_M, "BM must equal WM * WARPS_M");
+    static_assert(BN == WN * WARPS_N, "BN must equal WN * WARPS_N");
+    static_assert(32 % LR == 0, "LR must divide 32");
+    static_assert(TN % 4 == 0, "TN must be a multiple of 4");
+    static_assert(BK % 4 == 0 && BK % AK == 0, "BK must be a multiple of 4 and of AK");
+    static_assert(AK == 1 || AK == 2 || AK == 4, "AK is 1, 2 or 4");
+    static_assert(STAGES >= 2, "at least two stages");
+};
+
+template <class Cfg>
+__device__ __forceinline__ void load_slice(const GemmArgs& a, float* sA, float* sB, int m0,
+                                           int n0, int k0, int tid) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, NT = Cfg::NT;
+    constexpr int LDAS = Cfg::LDAS, LDBS = Cfg::LDBS;
+    const int rows_left = a.M - m0;   // valid rows of this A tile: r < rows_left
+    const int k_left = a.K - k0;      // valid k of this slice:      c < k_left
+    const int cols_left = a.N - n0;   // valid columns of this B tile
+    if constexpr (Cfg::VEC == 4) {
+        // A: BM rows x BK/4 chunks of 16 bytes.
+        constexpr int CPR = BK / 4;
+        constexpr int CHUNKS = BM * CPR;
+#pragma unroll
+        for (int e0 = 0; e0 < CHUNKS; e0 += NT) {
+            const int e = e0 + tid;
+            if (CHUNKS % NT == 0 || e < CHUNKS) {
+                const int r = e / CPR, c = (e % CPR) * 4;
+                const bool ok = (r < rows_left) && (c < k_left);
+                const int bytes = ok ? min(16, (k_left - c) * 4) : 0;
+                const float* src = ok ? a.A + (m0 + r) * a.lda + (k0 + c) : a.A;
+                cp_async16(smem_addr(sA + r * LDAS + c), src, bytes);
+            }
+        }
+        // B: BK rows x BN/4 chunks.
+        constexpr int CPRB = BN / 4;
+        constexpr int CHUNKSB = BK * CPRB;
+#pragma unroll
+        for (int e0 = 0; e0 < CHUNKSB; e0 += NT) {
+            const int e = e0 + tid;
+            if (CHUNKSB % NT == 0 || e < CHUNKSB) {
+                const int r = e / CPRB, c = (e % CPRB) * 4;
+                const bool ok = (r < k_left) && (c < cols_left);
+                const int bytes = ok ? min(16, (cols_left - c) * 4) : 0;
+                const float* src = ok ? a.B + (k0 + r) * a.ldb + (n0 + c) : a.B;
+                cp_async16(smem_addr(sB + r * LDBS + c), src, bytes);
+            }
+        }
+    } else {
+        constexpr int ELEMS = BM * BK;
+#pragma unroll
+        for (int e0 = 0; e0 < ELEMS; e0 += NT) {
+            const int e = e0 + tid;
+            if (ELEMS % NT == 0 || e < ELEMS) {
+                const int r = e / BK, c = e % BK;
+                const bool ok = (r < rows_left) && (c < k_left);
+                const float* src = ok ? a.A + (m0 + r) * a.lda + (k0 + c) : a.A;
+                cp_async4(smem_addr(sA + r * LDAS + c), src, ok ? 4 : 0);
+            }
+        }
+        constexpr int ELEMSB = BK * BN;
+#pragma unroll
+        for (int e0 = 0; e0 < ELEMSB; e0 += NT) {
+            const int e = e0 + tid;
+            if (ELEMSB % NT == 0 || e < ELEMSB) {
+                const int r = e / BN, c = e % BN;
+                const bool ok = (r < k_left) && (c < cols_left);
+                const float* src = ok ? a.B + (k0 + r) * a.ldb + (n0 + c) : a.B;
+                cp_async4(smem_addr(sB + r * LDBS + c), src, ok ? 4 : 0);
+            }
+        }
+    }
+}
+
+// One BK-deep slice of rank-1 updates from shared memory into the registers.
+template <class Cfg, class AccT>
+__device__ __forceinline__ void compute_slice(const float* sA, const float* sB, int a_row0,
+                                              int b_col0, AccT& acc) {
+    constexpr int BK = Cfg::BK, TM = Cfg::TM, TN = Cfg::TN, AK = Cfg::AK;
+    constexpr int LR = Cfg::LR, LC = Cfg::LC, LDAS = Cfg::LDAS, LDBS = Cfg::LDBS;
+#pragma unroll
+    for (int kq = 0; kq < BK; kq += AK) {
+        float av[TM][AK];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const float* p = sA + (a_row0 + i * LR) * LDAS + kq;
+            if constexpr (AK == 4) {
+                const float4 t = *reinterpret_cast<const float4*>(p);
+                av[i][0] = t.x; av[i][1] = t.y; av[i][2] = t.z; av[i][3] = t.w;
+            } else if constexpr (AK == 2) {
+                const float2 t = *reinterpret_cast<const float2*>(p);
+                av[i][0] = t.x; av[i][1] = t.y;
+            } else {
+                av[i][0] = *p;
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < AK; ++kk) {
+            float4 b[TN / 4];
+#pragma unroll
+            for (int j4 = 0; j4 < TN / 4; ++j4)
+                b[j4] = *reinterpret_cast<const float4*>(sB + (kq + kk) * LDBS + b_col0 +
+                                                         j4 * LC * 4);
+            float ak[TM];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) ak[i] = av[i][kk];
+            acc.rank1(ak, b);
+        }
+    }
+}
+
+template <class Cfg, class AccT>
+__device__ __forceinline__ void store_tile(const GemmArgs& a, const AccT& acc, int m0, int n0,
+                                           int a_row0, int b_col0) {
+    constexpr int TM = Cfg::TM, TN = Cfg::TN, LR = Cfg::LR, LC = Cfg::LC;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int gm = m0 + a_row0 + i * LR;
+        if (gm >= a.M) continue;
+        float* crow = a.C + gm * a.ldc;
+#pragma unroll
+        for (int j4 = 0; j4 < TN / 4; ++j4) {
+            const int gn = n0 + b_col0 + j4 * LC * 4;
+            const float4 v = acc.chunk(i, j4);
+            if (a.c_vec && gn + 3 < a.N) {
+                *reinterpret_cast<float4*>(crow + gn) = v;
+            } else {
+                if (gn + 0 < a.N) crow[gn + 0] = v.x;
+                if (gn + 1 < a.N) crow[gn + 1] = v.y;
+                if (gn + 2 < a.N) crow[gn + 2] = v.z;
+                if (gn + 3 < a.N) crow[gn + 3] = v.w;
+            }
+        }
+    }
+}
+
+// Split tile: write this CTA's partial sum of the tile (tile-local row-major
+// BM x BN floats) to its workspace slot.  sk_reduce_kernel adds the partials up.
+template <class Cfg, class AccT>
+__device__ __forceinline__ void store_partial(const GemmArgs& a, const CtaWork& w,
+                                              const Cursor& cur, const AccT& acc, int a_row0,
+                                              int b_col0) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, TM = Cfg::TM, TN = Cfg::TN;
+    constexpr int LR = Cfg::LR, LC = Cfg::LC;
+    const int t = cur.tile - w.dp_tiles;           // index among split tiles
+    float* P = a.ws_partial + (static_cast<long long>(w.g) * 2 + sk_slot(w, t)) * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j4 = 0; j4 < TN / 4; ++j4)
+            __stcg(reinterpret_cast<float4*>(P + (a_row0 + i * LR) * BN + b_col0 + j4 * LC * 4),
+                   acc.chunk(i, j4));
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const GemmArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    constexpr int STAGES = Cfg::STAGES, BK = Cfg::BK;
+    using AccT = Acc<Cfg::TM, Cfg::TN, Cfg::FMA2>;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int warp_m = warp / Cfg::WARPS_N, warp_n = warp % Cfg::WARPS_N;
+    // Lane -> (lr, lc).  Each quarter-warp (8 lanes, the unit a 16-byte shared
+    // load is served in) holds LRQ lane-rows x LCQ lane-columns, so one LDS.128
+    // of a quarter-warp touches at most LRQ distinct A rows or LCQ adjacent B
+    // chunks, in disjoint banks, and is served at the broadcast rate.
+    constexpr int LRQ = Cfg::LR < 8 ? Cfg::LR : 8;
+    constexpr int LCQ = 8 / LRQ;
+    const int q = lane >> 3, li = lane & 7;
+    const int lr = (q % (Cfg::LR / LRQ)) * LRQ + li % LRQ;
+    const int lc = (q / (Cfg::LR / LRQ)) * LCQ + li / LRQ;
+    // First A row / B column of this thread inside the CTA tile.  Rows are
+    // interleaved by LR, column chunks by LC*4.
+    const int a_row0 = warp_m * Cfg::WM + lr;
+    const int b_col0 = warp_n * Cfg::WN + lc * 4;
+
+    const CtaWork w = make_work(a, blockIdx.x);
+    if (w.total <= 0) return;
+
+    float* const sA0 = smem;
+    float* const sB0 = smem + STAGES * Cfg::A_STAGE;
+
+    Cursor ld;
+    ld.seek(w, 0);
+    Cursor cp = ld;
+
+    // Prologue: fill STAGES-1 slices.
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (ld.c < w.total) {
+            int m0, n0;
+            tile_origin(a, ld.tile, Cfg::BM, Cfg::BN, m0, n0);
+            load_slice<Cfg>(a, sA0 + s * Cfg::A_STAGE, sB0 + s * Cfg::B_STAGE, m0, n0,
+                            ld.kt * BK, tid);
+            ld.advance(w);
+        }
+        cp_async_commit();
+    }
+
+    AccT acc;
+    acc.zero();
+    int stage = 0;
+    int m0c, n0c;
+    tile_origin(a, cp.tile, Cfg::BM, Cfg::BN, m0c, n0c);
+
+    for (long long c = 0; c < w.total; ++c) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        // Refill the slot computed in the previous iteration.
+        if (ld.c < w.total) {
+            const int ls = (stage + STAGES - 1) % STAGES;
+            int m0, n0;
+            tile_origin(a, ld.tile, Cfg::BM, Cfg::BN, m0, n0);
+            load_slice<Cfg>(a, sA0 + ls * Cfg::A_STAGE, sB0 + ls * Cfg::B_STAGE, m0, n0,
+                            ld.kt * BK, tid);
+            ld.advance(w);
+        }
+        cp_async_commit();
+
+        compute_slice<Cfg>(sA0 + stage * Cfg::A_STAGE, sB0 + stage * Cfg::B_STAGE, a_row0,
+                           b_col0, acc);
+        stage = (stage + 1 == STAGES) ? 0 : stage + 1;
+
+        if (cp.kt + 1 == cp.kt_end) {
+            if (cp.kt_begin == 0 && cp.kt_end == w.KT)
+                store_tile<Cfg>(a, acc, m0c, n0c, a_row0, b_col0);
+            else
+                store_partial<Cfg>(a, w, cp, acc, a_row0, b_col0);
+            acc.zero();
+            cp.advance(w);
+            if (cp.c < w.total) tile_origin(a, cp.tile, Cfg::BM, Cfg::BN, m0c, n0c);
+        } else {
+            cp.advance(w);
+        }
+    }
+    cp_async_wait<0>();
+}
+
+template <class Cfg>
+constexpr KernelEntry make_entry(const char* name) {
+    return KernelEntry{name,
+                       reinterpret_cast<const void*>(&sgemm_ffma_kernel<Cfg>),
+                       Cfg::BM, Cfg::BN, Cfg::BK, Cfg::WM, Cfg::WN, Cfg::TM, Cfg::TN,
+                       Cfg::STAGES, Cfg::NT, Cfg::SMEM_BYTES, Cfg::VEC, Cfg::FMA2 ? 1 : 0};
+}
+
+}  // namespace sgemm

@@ -1,0 +1,46 @@
+// Internal types shared by the host dispatcher and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sgemm.h"
+
+namespace sgemm {
+
+// Everything one launch needs, passed by value in the kernel parameter space.
+struct GemmArgs {
+    int M, N, K;
+    const float* A;
+    const float* B;
+    float* C;
+    long long lda, ldb, ldc;
+    int c_vec;            // 1: C and ldc allow 16-byte stores
+
+    // Tile grid and schedule (see the persistent scheduler in sgemm_ffma.cuh).
+    int tiles_m, tiles_n;  // ceil(M/BM), ceil(N/BN)
+    int KT;                // k-tiles per output tile: ceil(K/BK)
+    int grid;              // CTAs launched (G)
+    int dp_tiles;          // tiles [0, dp_tiles) are done whole by one CTA each
+    int sk_tiles;          // tiles [dp_tiles, dp_tiles + sk_tiles) are split over CTAs
+    long long sk_iters;    // sk_tiles * KT: k-tiles shared out over the G CTAs
+    int group_m;           // tile rasterisation: tile rows per group
+
+    float* ws_partial;     // [G][2][BM*BN] partial tiles of split tiles
+};
+
+// One entry of the tile table.
+struct KernelEntry {
+    const char* name;
+    const void* kernel;     // __global__ void(GemmArgs)
+    int bm, bn, bk, wm, wn, tm, tn, stages, threads, smem_bytes;
+    int vec;                // 4: needs 16-byte aligned A/B rows; 1: any alignment
+    int fma2;
+};
+
+// Sums the partial tiles of a stream-K launch into C (sgemm_reduce.cu).  Launch
+// it on the same stream right after the main kernel when a.sk_tiles > 0.
+cudaError_t launch_sk_reduce(const GemmArgs& a, int bm, int bn, int sms, cudaStream_t stream);
+int reduce_chunks(int bm, int bn, int sk_tiles, int sms);
+
+}  // namespace sgemm

@@ -1,0 +1,31 @@
+// Tile-table entries with 16-byte global loads (rows 16-byte aligned): the
+// large-tile FFMA2 kernels.
+#include "sgemm_ffma.cuh"
+
+namespace sgemm {
+
+// FfmaCfg<BM, BN, BK, TM, TN, LR, WARPS_M, WARPS_N, STAGES, VEC, AK, FMA2, MINB>
+// One 256-thread CTA per SM with 8 x 16 register tiles (255 registers): the
+// large-problem workhorses; BK = 64 halves the per-slice overhead when K is long.
+using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 4, true, 1>;
+using W256K32 = FfmaCfg<128, 256, 32, 8, 16, 4, 4, 2, 4, 4, 4, true, 1>;
+using H256K64 = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1>;
+// Two CTAs per SM with 8 x 8 tiles (128 registers).
+using S128K32 = FfmaCfg<128, 128, 32, 8, 8, 4, 4, 2, 3, 4, 4, true, 2>;
+// Scalar-FFMA counterpart of the same tile, kept for comparison with fma.rn.f32x2.
+using S128F1 = FfmaCfg<128, 128, 16, 8, 8, 4, 4, 2, 4, 4, 4, false, 2>;
+
+static const KernelEntry kEntries[] = {
+    make_entry<W256K64>("128x256x64_t8x16_s2_f2_v4"),
+    make_entry<W256K32>("128x256x32_t8x16_s4_f2_v4"),
+    make_entry<H256K64>("256x128x64_t8x16_s2_f2_v4"),
+    make_entry<S128K32>("128x128x32_t8x8_s3_f2_v4"),
+    make_entry<S128F1>("128x128x16_t8x8_s4_f1_v4"),
+};
+
+const KernelEntry* ffma_entries_main(int* count) {
+    *count = static_cast<int>(sizeof(kEntries) / sizeof(kEntries[0]));
+    return kEntries;
+}
+
+}  // namespace sgemm

@@ -1,0 +1,92 @@
+// Second phase of a stream-K launch: sums the partial tiles of every split tile.
+//
+// Each CTA of the main kernel that worked on part of a split tile's K range
+// wrote its partial BM x BN sum to its own workspace slot.  Here every split
+// tile is cut into `chunks` pieces and each piece is reduced by one CTA, so all
+// SMs share the (L2-resident) partial data.  Partials are added in increasing
+// CTA order, i.e. in increasing k, which fixes the summation order: the result
+// does not depend on timing.  The schedule formulas are the ones the main
+// kernel used (sgemm_sched.cuh).
+#include "sgemm_internal.h"
+#include "sgemm_sched.cuh"
+
+namespace sgemm {
+
+namespace {
+
+constexpr int kReduceThreads = 256;
+constexpr int kBatch = 8;
+
+__global__ void __launch_bounds__(kReduceThreads) sk_reduce_kernel(const GemmArgs a, int bm,
+                                                                   int bn, int chunks) {
+    __shared__ const float4* s_src[kMaxSplit];
+    const int t = blockIdx.x / chunks, part = blockIdx.x - t * chunks;
+    const long long tb = static_cast<long long>(t) * a.KT;
+    const int g0 = sk_owner(tb, a.grid, a.sk_iters);
+    const int g1 = sk_owner(tb + a.KT - 1, a.grid, a.sk_iters);
+    const int n = g1 - g0 + 1;  // contributors, in increasing k order
+    if (n <= 1) return;         // one CTA held the whole K range and stored the tile itself
+    const long long tile_floats = static_cast<long long>(bm) * bn;
+    for (int i = threadIdx.x; i < n; i += kReduceThreads) {
+        const int gg = g0 + i;
+        const int slot = t - static_cast<int>((a.sk_iters * gg / a.grid) / a.KT);
+        s_src[i] = reinterpret_cast<const float4*>(
+            a.ws_partial + (static_cast<long long>(gg) * 2 + slot) * tile_floats);
+    }
+    __syncthreads();
+    int m0, n0;
+    tile_origin(a, a.dp_tiles + t, bm, bn, m0, n0);
+    const int n4 = bm * bn / 4;  // float4 per tile
+    const int per = (n4 + chunks - 1) / chunks;
+    const int e_end = min(n4, (part + 1) * per);
+    for (int e = part * per + threadIdx.x; e < e_end; e += kReduceThreads) {
+        // Up to kBatch loads in flight per thread; the additions still follow
+        // contributor order 0, 1, 2, ... exactly.
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i0 = 0; i0 < n; i0 += kBatch) {
+            float4 q[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (i0 + j < n) q[j] = __ldcg(s_src[i0 + j] + e);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (i0 + j < n) {
+                    s.x += q[j].x;
+                    s.y += q[j].y;
+                    s.z += q[j].z;
+                    s.w += q[j].w;
+                }
+        }
+        const int r = (4 * e) / bn, c = (4 * e) - r * bn;
+        const int gm = m0 + r, gn = n0 + c;
+        if (gm >= a.M) continue;
+        float* crow = a.C + gm * a.ldc;
+        if (a.c_vec && gn + 3 < a.N) {
+            *reinterpret_cast<float4*>(crow + gn) = s;
+        } else {
+            if (gn + 0 < a.N) crow[gn + 0] = s.x;
+            if (gn + 1 < a.N) crow[gn + 1] = s.y;
+            if (gn + 2 < a.N) crow[gn + 2] = s.z;
+            if (gn + 3 < a.N) crow[gn + 3] = s.w;
+        }
+    }
+}
+
+}  // namespace
+
+int reduce_chunks(int bm, int bn, int sk_tiles, int sms) {
+    const int n4 = bm * bn / 4;
+    int chunks = (4 * sms + sk_tiles - 1) / sk_tiles;          // about four CTAs per SM
+    const int max_chunks = (n4 + kReduceThreads - 1) / kReduceThreads;
+    if (chunks > max_chunks) chunks = max_chunks;
+    return chunks < 1 ? 1 : chunks;
+}
+
+cudaError_t launch_sk_reduce(const GemmArgs& a, int bm, int bn, int sms, cudaStream_t stream) {
+    const int chunks = reduce_chunks(bm, bn, a.sk_tiles, sms);
+    sk_reduce_kernel<<<static_cast<unsigned>(a.sk_tiles) * chunks, kReduceThreads, 0, stream>>>(
+        a, bm, bn, chunks);
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm

@@ -1,0 +1,167 @@
+/*
+ * sgemm.h -- C ABI of the GB300 FP32 matrix-multiply library (libsgemm_gb300.so).
+ *
+ * The library computes the row-major FP32 product
+ *
+ *     C[i,j] = sum_{k=0}^{K-1} A[i,k] * B[k,j]        0 <= i < M, 0 <= j < N
+ *
+ * ("Micro Kernel 입문하기", §3, the GEMM formula held by the c_ij accumulators;
+ *  "누산 개념을 Grid-Block-Warp-Thread 계층에 끼워넣기", §1-§2: one kernel launch
+ *  completes all of C, each block owning a BM x BN tile of C, each warp a warp
+ *  tile and each thread a TM x TN register tile accumulated over BK-deep
+ *  shared-memory slices; "Register/Shared Memory Tiling", 동작 원리.)
+ *
+ * Layout.  Every matrix is row-major with a leading dimension counted in
+ * elements: A[i,k] = A[i*lda + k], B[k,j] = B[k*ldb + j], C[i,j] = C[i*ldc + j]
+ * (the pages' `A[gm * p.lda + gk]` and `C[m * p.ldd + n]`, "기존 작성한 GE_v2 의
+ * regemm 타일드 커널의 1:1 매핑, gemm_tiled_test 작성", §3 and §6).
+ *
+ * Semantics.  C is overwritten (beta = 0, alpha = 1).  Elements of C outside the
+ * M x N region, including the padding between rows when ldc > N, are never
+ * written; elements of A and B outside their logical extents are never read
+ * (the tile loads substitute zeros there, ibid. §3 "boundary check 후 0-padding").
+ * K == 0 writes zeros to C (the empty sum).  M == 0 or N == 0 is a no-op.
+ *
+ * Memory.  A, B and C are DEVICE pointers owned by the caller.  C must not
+ * overlap A or B.  Any alignment of pointers and leading dimensions is accepted;
+ * 16-byte-aligned operands with leading dimensions that are multiples of 4 take
+ * the vectorised kernels, others a 4-byte-granular variant.
+ *
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ * call is asynchronous on that stream and does not synchronise the host.
+ *
+ * Errors.  Every entry point returns an sgemm_status and never aborts the
+ * process.  Invalid arguments are rejected before anything is launched.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SGEMM_API __attribute__((visibility("default")))
+#else
+#define SGEMM_API
+#endif
+
+struct CUstream_st;                       /* cudaStream_t == struct CUstream_st* */
+typedef struct CUstream_st* sgemm_stream_t;
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_INVALID_ARG = -1,   /* bad size, leading dimension, null or aliased pointer */
+    SGEMM_ERR_ALIGNMENT = -2,     /* reserved: misalignment selects another kernel instead */
+    SGEMM_ERR_LAUNCH = -3,        /* a CUDA call failed (message: sgemm_last_error()) */
+    SGEMM_ERR_UNSUPPORTED = -4,   /* no device, wrong architecture, unknown kernel id */
+    SGEMM_ERR_TIMEOUT = -5,       /* a bounded device-side wait gave up */
+    SGEMM_ERR_WORKSPACE = -6      /* caller workspace too small, or allocation failed */
+} sgemm_status;
+
+/* One entry of the tile table, as chosen for a problem.  `kernel_id` indexes the
+ * table (0 .. sgemm_num_kernels()-1).  `split_k` is the number of CTAs that share
+ * the K range of a split tile (1 = data-parallel only); `grid` the CTAs launched
+ * (a persistent grid); `sk_tiles` the tiles finished by several CTAs. */
+typedef struct {
+    int bm, bn, bk;        /* block tile of C and depth of one shared-memory slice */
+    int wm, wn;            /* warp tile */
+    int tm, tn;            /* register tile of one thread */
+    int stages;            /* shared-memory pipeline depth */
+    int threads;           /* threads per CTA */
+    int smem_bytes;        /* dynamic shared memory per CTA */
+    int split_k;           /* max CTAs sharing one tile's K range (1 = none) */
+    int kernel_id;         /* index into the tile table */
+    int vec;               /* 4: 16-byte global loads; 1: 4-byte loads (any alignment) */
+    int grid;              /* CTAs launched */
+    int tiles;             /* BM x BN tiles of C */
+    int sk_tiles;          /* tiles completed by more than one CTA (stream-K) */
+    int ctas_per_sm;       /* resident CTAs per SM for this kernel */
+    int fma2;              /* 1: packed fma.rn.f32x2 micro-kernel */
+} sgemm_config;
+
+/* C = A.B on `stream`.  One kernel launch, plus a second, short reduction launch
+ * when the schedule splits the K range of some tiles between CTAs (stream-K);
+ * the partial tiles then go to a library-owned device workspace (allocated on
+ * first use per device and stream with the stream-ordered allocator, grown when
+ * a larger one is needed, freed by sgemm_shutdown).  The first call that needs
+ * a workspace must not be made while the stream is being captured into a CUDA
+ * graph. */
+SGEMM_API int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+              float* C, int ldc, sgemm_stream_t stream);
+
+/* As sgemm_run, with a caller-owned device workspace of `ws_bytes` bytes (at least
+ * sgemm_workspace_size() for the same arguments, 16-byte aligned; may be NULL
+ * when that size is 0).  The library allocates nothing on this path.  The
+ * workspace needs no initialisation; it must stay untouched by other work while
+ * the call runs and must not be shared by calls that can overlap on the GPU.
+ * Returns SGEMM_ERR_WORKSPACE if it is missing or too small. */
+SGEMM_API int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                 float* C, int ldc, void* ws, size_t ws_bytes, sgemm_stream_t stream);
+
+/* Bytes of workspace sgemm_run_ws needs for these arguments (0 if none). */
+SGEMM_API int sgemm_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
+                         const float* A, const float* B, const float* C, size_t* out_bytes);
+
+/* As sgemm_run, forcing tile-table entry `kernel_id` (for tests and tuning) and a
+ * schedule: `schedule` 0 = automatic, 1 = data-parallel only, 2 = stream-K on the
+ * last partial wave whenever it has at least one k-tile per CTA.  Returns
+ * SGEMM_ERR_UNSUPPORTED if that entry cannot serve these operands (e.g. a
+ * 16-byte-load entry for unaligned operands). */
+SGEMM_API int sgemm_run_with(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                   float* C, int ldc, int kernel_id, int schedule, sgemm_stream_t stream);
+
+/* The configuration sgemm_run would use for these arguments on the current
+ * device.  Pointers only matter through their alignment; pass NULL to assume
+ * 16-byte-aligned operands. */
+SGEMM_API int sgemm_query_config(int M, int N, int K, int lda, int ldb, int ldc,
+                       const float* A, const float* B, const float* C, sgemm_config* out);
+
+/* Host-buffer convenience for end-to-end use: copies A and B from host memory
+ * (pinned for full speed) into the caller's device buffers dA, dB (row-major,
+ * leading dimensions lda, ldb), runs sgemm_run into dC (leading dimension ldc),
+ * and copies C back to hC, all on `stream`.  The call returns when the work is
+ * queued; synchronise the stream before reading hC. */
+SGEMM_API int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* hB, int ldb,
+                   float* hC, int ldc, float* dA, float* dB, float* dC,
+                   sgemm_stream_t stream);
+
+/* Host-only check of the persistent / stream-K schedule (no GPU needed): plans
+ * M x N x K for tile-table entry `kernel_id` as if `sms` SMs each held
+ * `ctas_per_sm` CTAs, then walks every CTA's list of k-slices the way the kernel
+ * does.  Returns SGEMM_OK if every (tile, k-slice) is computed exactly once and
+ * every split tile's partial slots and contributor count are consistent, else
+ * SGEMM_ERR_INVALID_ARG with the reason in sgemm_last_error().  `out` (may be
+ * NULL) receives the planned configuration. */
+SGEMM_API int sgemm_schedule_check(int M, int N, int K, int kernel_id, int sms, int ctas_per_sm,
+                                   int schedule, sgemm_config* out);
+
+/* Number of entries in the tile table, and entry `kernel_id`'s static shape
+ * (grid, tiles, sk_tiles and split_k are left 0). */
+SGEMM_API int sgemm_num_kernels(void);
+SGEMM_API int sgemm_kernel_info(int kernel_id, sgemm_config* out);
+
+/* Name of tile-table entry `kernel_id` ("" if out of range; static storage). */
+SGEMM_API const char* sgemm_kernel_name(int kernel_id);
+
+/* Human-readable name of a status code (static storage). */
+SGEMM_API const char* sgemm_status_string(int status);
+
+/* Text of the last CUDA error seen by this thread (static per-thread storage). */
+SGEMM_API const char* sgemm_last_error(void);
+
+/* Kernels this library has launched in this process (for launch accounting). */
+SGEMM_API uint64_t sgemm_launch_count(void);
+
+/* Frees the library-owned workspaces on every device.  Not thread-safe with
+ * concurrent sgemm_run calls; call it when the library is no longer in use. */
+SGEMM_API int sgemm_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

@@ -1,0 +1,129 @@
+"""The C-ABI library: it loads, exports every symbol include/sgemm.h declares,
+and rejects bad arguments before touching the GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import REPO
+
+HEADER = os.path.join(REPO, "include", "sgemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SGEMM_API\s+[\w\s\*]+?\b(sgemm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("sgemm_run", "sgemm_query_config", "sgemm_status_string", "sgemm_run_ws",
+                 "sgemm_workspace_size", "sgemm_run_host"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol():
+    from dense_fp32_gemm_09_gb300 import _abi
+    assert set(_abi.SIGNATURES) == set(declared_functions())
+
+
+def test_config_struct_matches_header():
+    from dense_fp32_gemm_09_gb300 import _abi
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} sgemm_config;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = re.findall(r"\b(\w+)\s*[,;]", body)
+    assert [f for f, _ in _abi.SgemmConfig._fields_] == fields
+
+
+def test_status_strings(lib):
+    assert lib.sgemm_status_string(0) == b"SGEMM_OK"
+    assert lib.sgemm_status_string(-1) == b"SGEMM_ERR_INVALID_ARG"
+    assert lib.sgemm_status_string(-6) == b"SGEMM_ERR_WORKSPACE"
+    assert lib.sgemm_status_string(12345) == b"SGEMM_ERR_UNKNOWN"
+
+
+def test_kernel_table_static_info(lib):
+    from dense_fp32_gemm_09_gb300._abi import SgemmConfig
+    n = lib.sgemm_num_kernels()
+    assert n >= 3
+    names = set()
+    for i in range(n):
+        cfg = SgemmConfig()
+        assert lib.sgemm_kernel_info(i, ctypes.byref(cfg)) == 0
+        assert cfg.bm % cfg.wm == 0 and cfg.bn % cfg.wn == 0
+        assert cfg.threads == 32 * (cfg.bm // cfg.wm) * (cfg.bn // cfg.wn)
+        assert cfg.wm * cfg.wn == 32 * cfg.tm * cfg.tn
+        assert cfg.vec in (1, 4)
+        names.add(lib.sgemm_kernel_name(i))
+    assert len(names) == n
+    assert lib.sgemm_kernel_info(n, ctypes.byref(SgemmConfig())) == -4
+    assert lib.sgemm_kernel_name(n) == b""
+
+
+P = 0x10000  # a 16-byte-aligned fake device address: these calls never launch
+
+
+@pytest.mark.parametrize("args", [
+    (-1, 4, 4, P, 4, P, 4, P * 8, 4),          # negative M
+    (4, -1, 4, P, 4, P, 4, P * 8, 4),          # negative N
+    (4, 4, -1, P, 4, P, 4, P * 8, 4),          # negative K
+    (4, 4, 8, P, 7, P, 4, P * 8, 4),           # lda < K
+    (4, 4, 4, P, 4, P, 3, P * 8, 4),           # ldb < N
+    (4, 4, 4, P, 4, P, 4, P * 8, 3),           # ldc < N
+    (4, 4, 4, 0, 4, P, 4, P * 8, 4),           # null A
+    (4, 4, 4, P, 4, 0, 4, P * 8, 4),           # null B
+    (4, 4, 4, P, 4, P * 4, 4, 0, 4),           # null C
+    (4, 4, 4, P, 4, P * 4, 4, P + 8, 4),       # C overlaps A
+    (4, 4, 4, P * 64, 4, P, 4, P + 16, 4),     # C overlaps B
+])
+def test_invalid_arguments_rejected_before_launch(lib, args):
+    assert lib.sgemm_run(*args, None) == -1
+    assert lib.sgemm_run_with(*args, -1, 0, None) == -1
+    assert lib.sgemm_run_ws(*args, None, 0, None) == -1
+    assert lib.sgemm_last_error() != b""
+
+
+def test_empty_output_is_a_noop(lib):
+    assert lib.sgemm_run(0, 5, 3, P, 3, P * 4, 5, P * 8, 5, None) == 0
+    assert lib.sgemm_run(5, 0, 3, P, 3, P * 4, 1, P * 8, 1, None) == 0
+    assert lib.sgemm_run(0, 0, 0, 0, 1, 0, 1, 0, 1, None) == 0
+
+
+def test_bad_kernel_or_schedule(lib):
+    assert lib.sgemm_run_with(4, 4, 4, P, 4, P * 4, 4, P * 8, 4, -7, 0, None) == -4
+    assert lib.sgemm_run_with(4, 4, 4, P, 4, P * 4, 4, P * 8, 4, 0, 9, None) == -1
+
+
+def test_workspace_size_rejects_bad_sizes(lib):
+    out = ctypes.c_size_t(99)
+    assert lib.sgemm_workspace_size(-1, 4, 4, 4, 4, 4, None, None, None, ctypes.byref(out)) == -1
+    assert lib.sgemm_workspace_size(4, 4, 0, 1, 4, 4, None, None, None, ctypes.byref(out)) == 0
+    assert out.value == 0
+
+
+def test_product_path_does_not_reference_the_oracle():
+    """The library sources and the binding never name the oracle package."""
+    pkg = os.path.join(REPO, "dense_fp32_gemm_09_gb300")
+    for root, _, files in os.walk(pkg):
+        if "_lib" in root:
+            continue
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(root, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text and "sgemm_oracle" not in text, f
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    from dense_fp32_gemm_09_gb300 import _abi
+    monkeypatch.setattr(_abi, "_lib", None)
+    monkeypatch.setattr(_abi, "library_path", lambda: str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _abi.load()

@@ -1,0 +1,306 @@
+"""Parity of the CUDA path (called through the C ABI) with the fp64 CPU oracle.
+
+Tolerance for FP32 results: max |C_gpu - C_ref| <= 1e-6 * K * max|A| * max|B|,
+with the maxima over the drawn inputs.  Where the arithmetic is exact in any
+summation order (small integers, identity and permutation matrices) the bar is
+bit equality with the oracle rounded to fp32.
+"""
+import numpy as np
+import pytest
+
+from dense_fp32_gemm_09_gb300 import kernel_table, sgemm, sgemm_query_config
+from dense_fp32_gemm_09_gb300.workloads import (WORKLOADS, make_inputs, random_pair,
+                                                small_int_pair)
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 1234.5
+
+
+def tolerance(A, B):
+    K = A.shape[1]
+    return 1e-6 * K * float(A.abs().max()) * float(B.abs().max())
+
+
+def canaried(torch, M, N, ldc_pad=5, rows_pad=2):
+    """An (M, N) view with leading dimension N + ldc_pad inside a sentinel-filled
+    buffer with rows_pad extra rows above and below."""
+    buf = torch.full((M + 2 * rows_pad, N + ldc_pad), SENTINEL, dtype=torch.float32,
+                     device="cuda")
+    return buf, buf[rows_pad:rows_pad + M, :N]
+
+
+def check_canary(buf, M, N, rows_pad=2):
+    b = buf.cpu().numpy()
+    mask = np.ones(b.shape, dtype=bool)
+    mask[rows_pad:rows_pad + M, :N] = False
+    assert np.all(b[mask] == SENTINEL), "a write landed outside the M x N region"
+
+
+def padded(torch, X, pad, offset=0):
+    """X copied into a device buffer with leading dimension cols + pad, starting
+    `offset` elements into the buffer (offset 1 breaks 16-byte alignment)."""
+    rows, cols = X.shape
+    ld = cols + pad
+    flat = torch.full((offset + rows * ld + 8,), float("nan"), dtype=torch.float32,
+                      device="cuda")
+    view = flat[offset:offset + rows * ld].view(rows, ld)[:, :cols]
+    view.copy_(X)
+    return view
+
+
+# --------------------------------------------------------------------------
+# the named workloads, in the configuration sgemm_run picks (the bench's)
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("name", ["sgemm_256", "sgemm_1024", "sgemm_2048",
+                                  "sgemm_ragged_3001x2047x1999"])
+def test_workload_full_parity(cuda, oracle_mod, name):
+    torch = cuda
+    A, B = make_inputs(name)
+    C = sgemm(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+    err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+    assert err <= tolerance(A, B), (name, err, tolerance(A, B))
+
+
+@pytest.mark.parametrize("name", ["sgemm_4096", "sgemm_8192", "sgemm_tall_16384x64x4096"])
+def test_workload_sampled_rows(cuda, oracle_mod, name):
+    torch = cuda
+    w = WORKLOADS[name]
+    A, B = make_inputs(name)
+    C = sgemm(A.cuda(), B.cuda())
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(12345)
+    rows = np.unique(np.concatenate([[0, w.M - 1], rng.integers(0, w.M, 48)])).astype(np.int32)
+    ref = oracle_mod.gemm_f64_rows(A.numpy(), B.numpy(), rows)
+    got = C[torch.from_numpy(rows.astype(np.int64)).cuda()].cpu().numpy().astype(np.float64)
+    err = np.max(np.abs(got - ref))
+    assert err <= tolerance(A, B), (name, err, tolerance(A, B))
+    assert torch.isfinite(C).all()
+
+
+def test_tall_skinny_full_parity(cuda, oracle_mod):
+    A, B = make_inputs("sgemm_tall_16384x64x4096")
+    C = sgemm(A.cuda(), B.cuda()).cpu().numpy().astype(np.float64)
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+    assert np.max(np.abs(C - ref)) <= tolerance(A, B)
+
+
+# --------------------------------------------------------------------------
+# every tile-table entry, both schedules, ragged shapes, canaried output
+# --------------------------------------------------------------------------
+
+SHAPES = [(1, 1, 1), (3, 5, 7), (9, 4, 2), (31, 33, 17), (65, 63, 129), (127, 129, 65),
+          (129, 127, 300), (257, 383, 1000), (300, 260, 33), (1000, 70, 517)]
+
+
+def _ids():
+    try:
+        return [k["name"] for k in kernel_table()]
+    except Exception:   # library not built: the test fixture reports it
+        return []
+
+
+@pytest.mark.parametrize("kname", _ids())
+@pytest.mark.parametrize("schedule", [1, 2])
+def test_each_kernel_ragged_shapes(cuda, oracle_mod, kname, schedule):
+    torch = cuda
+    table = {k["name"]: k for k in kernel_table()}
+    kid = table[kname]["kernel_id"]
+    for (M, N, K) in SHAPES:
+        A, B = random_pair(M, N, K, seed=M * 7 + N * 3 + K)
+        # ld padded to a multiple of 4 so that 16-byte entries may run too
+        dA = padded(torch, A, (-K) % 4 + 4)
+        dB = padded(torch, B, (-N) % 4 + 4)
+        buf, C = canaried(torch, M, N, ldc_pad=(-N) % 4 + 4)
+        sgemm(dA, dB, out=C, kernel_id=kid, schedule=schedule)
+        torch.cuda.synchronize()
+        check_canary(buf, M, N)
+        ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+        err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+        assert err <= tolerance(A, B), (kname, schedule, (M, N, K), err)
+
+
+@pytest.mark.parametrize("kname", [k for k in _ids() if k.endswith("_v1")])
+def test_unaligned_operands(cuda, oracle_mod, kname):
+    torch = cuda
+    kid = {k["name"]: k for k in kernel_table()}[kname]["kernel_id"]
+    for (M, N, K) in [(33, 17, 65), (130, 131, 129), (301, 205, 199)]:
+        A, B = random_pair(M, N, K, seed=K)
+        dA = padded(torch, A, 1, offset=1)     # odd lda, 4-byte aligned base
+        dB = padded(torch, B, 3, offset=3)
+        buf, C = canaried(torch, M, N, ldc_pad=1)
+        sgemm(dA, dB, out=C, kernel_id=kid, schedule=2)
+        torch.cuda.synchronize()
+        check_canary(buf, M, N)
+        ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+        err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+        assert err <= tolerance(A, B)
+
+
+def test_vec4_entry_refuses_unaligned(cuda):
+    torch = cuda
+    from dense_fp32_gemm_09_gb300 import SgemmError
+    kid = [k for k in kernel_table() if k["vec"] == 4][0]["kernel_id"]
+    A, B = random_pair(8, 8, 9, seed=0)
+    with pytest.raises(SgemmError, match="UNSUPPORTED"):
+        sgemm(A.cuda(), B.cuda(), kernel_id=kid)
+
+
+# --------------------------------------------------------------------------
+# exact cases: bit equality
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("M,N,K", [(3001, 2047, 1999), (512, 640, 4096), (77, 1031, 263)])
+def test_small_integers_bit_exact(cuda, oracle_mod, M, N, K):
+    A, B = small_int_pair(M, N, K, seed=M + N + K)
+    C = sgemm(A.cuda(), B.cuda()).cpu().numpy()
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy()).astype(np.float32)
+    assert np.array_equal(C, ref)
+
+
+@pytest.mark.parametrize("n,cols", [(129, 77), (1000, 333)])
+def test_identity_and_permutation_bit_exact(cuda, n, cols):
+    torch = cuda
+    g = torch.Generator().manual_seed(n)
+    X = torch.randn(n, cols, generator=g)
+    I = torch.eye(n)
+    assert torch.equal(sgemm(I.cuda(), X.cuda()).cpu(), X)
+    perm = torch.randperm(n, generator=g)
+    P = torch.zeros(n, n)
+    P[torch.arange(n), perm] = 1.0
+    assert torch.equal(sgemm(P.cuda(), X.cuda()).cpu(), X[perm])
+    Y = torch.randn(cols, n, generator=g)
+    assert torch.equal(sgemm(Y.cuda(), P.cuda()).cpu(), Y[:, torch.argsort(perm)])
+
+
+def test_ones_give_K(cuda):
+    torch = cuda
+    for M, N, K in [(1, 1, 1), (200, 300, 4097), (5, 64, 12345)]:
+        C = sgemm(torch.ones(M, K, device="cuda"), torch.ones(K, N, device="cuda"))
+        assert torch.all(C == K)
+
+
+# --------------------------------------------------------------------------
+# degenerate sizes, determinism, entry points
+# --------------------------------------------------------------------------
+
+
+def test_zero_K_writes_zeros_only_inside(cuda):
+    torch = cuda
+    buf, C = canaried(torch, 37, 45)
+    A = torch.empty(37, 0, device="cuda")
+    B = torch.empty(0, 45, device="cuda")
+    sgemm(A, B, out=C)
+    torch.cuda.synchronize()
+    check_canary(buf, 37, 45)
+    assert torch.all(C == 0)
+
+
+def test_empty_M_or_N(cuda):
+    torch = cuda
+    assert sgemm(torch.ones(0, 5, device="cuda"), torch.ones(5, 7, device="cuda")).shape == (0, 7)
+    assert sgemm(torch.ones(4, 5, device="cuda"), torch.ones(5, 0, device="cuda")).shape == (4, 0)
+
+
+def test_run_to_run_deterministic(cuda):
+    torch = cuda
+    A, B = make_inputs("sgemm_4096")
+    dA, dB = A.cuda(), B.cuda()
+    C1 = sgemm(dA, dB).clone()
+    C2 = sgemm(dA, dB)
+    assert torch.equal(C1, C2)
+    for kid in {k["kernel_id"] for k in kernel_table() if k["vec"] == 4}:
+        a = sgemm(dA[:1000, :3000], dB[:3000, :700], kernel_id=kid, schedule=2).clone()
+        b = sgemm(dA[:1000, :3000], dB[:3000, :700], kernel_id=kid, schedule=2)
+        assert torch.equal(a, b)
+
+
+def test_stream_k_matches_data_parallel_within_tolerance(cuda, oracle_mod):
+    torch = cuda
+    A, B = random_pair(700, 900, 2500, seed=9)
+    dA, dB = A.cuda(), B.cuda()
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+    for kid in {k["kernel_id"] for k in kernel_table() if k["vec"] == 4}:
+        for schedule in (1, 2):
+            C = sgemm(dA, dB, kernel_id=kid, schedule=schedule).cpu().numpy()
+            assert np.max(np.abs(C - ref)) <= tolerance(A, B)
+
+
+def test_caller_workspace_entry_point(cuda, oracle_mod):
+    torch = cuda
+    from dense_fp32_gemm_09_gb300 import check, sgemm_run_ws, sgemm_workspace_size
+    A, B = make_inputs("sgemm_1024")
+    M, K = A.shape
+    N = B.shape[1]
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty(M, N, device="cuda")
+    need = sgemm_workspace_size(M, N, K, K, N, N, dA.data_ptr(), dB.data_ptr(), C.data_ptr())
+    ws = torch.full((max(need, 16) // 4 + 64,), 7.0, device="cuda")   # dirty on purpose
+    for _ in range(2):
+        check(sgemm_run_ws(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, C.data_ptr(), N,
+                           ws.data_ptr(), ws.numel() * 4), "sgemm_run_ws")
+        torch.cuda.synchronize()
+        ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+        assert np.max(np.abs(C.cpu().numpy() - ref)) <= tolerance(A, B)
+    if need > 0:
+        st = sgemm_run_ws(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, C.data_ptr(), N,
+                          ws.data_ptr(), need - 4)
+        assert st == -6
+
+
+def test_library_workspace_reused_across_layouts(cuda, oracle_mod):
+    """Consecutive split-tile calls with different tile sizes and grids share the
+    library workspace on one stream; each must still be exact to tolerance."""
+    torch = cuda
+    table = {k["name"]: k["kernel_id"] for k in kernel_table()}
+    cases = [("128x256x64_t8x16_s2_f2_v4", (1500, 1700, 3000)),
+             ("128x64x16_t16x8_s4_f2_v4", (6000, 64, 2048)),
+             ("64x64x16_t4x4_s3_f1_v4", (300, 260, 3000)),
+             ("256x128x64_t8x16_s2_f2_v4", (700, 900, 5000))]
+    for rep in range(2):
+        for name, (M, N, K) in cases:
+            A, B = random_pair(M, N, K, seed=M + rep)
+            C = sgemm(A.cuda(), B.cuda(), kernel_id=table[name], schedule=2)
+            ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+            err = np.max(np.abs(C.cpu().numpy() - ref))
+            assert err <= tolerance(A, B), (name, (M, N, K), rep, err)
+
+
+def test_host_buffer_entry_point(cuda, oracle_mod):
+    torch = cuda
+    from dense_fp32_gemm_09_gb300 import check, sgemm_run_host
+    A, B = make_inputs("sgemm_ragged_3001x2047x1999")
+    M, K = A.shape
+    N = B.shape[1]
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.empty(M, N).pin_memory()
+    dA = torch.empty(M, K, device="cuda")
+    dB = torch.empty(K, N, device="cuda")
+    dC = torch.empty(M, N, device="cuda")
+    check(sgemm_run_host(M, N, K, hA.data_ptr(), K, hB.data_ptr(), N, hC.data_ptr(), N,
+                         dA.data_ptr(), dB.data_ptr(), dC.data_ptr()), "sgemm_run_host")
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+    assert np.max(np.abs(hC.numpy() - ref)) <= tolerance(A, B)
+
+
+def test_query_config_matches_bench_choice(cuda):
+    cfg = sgemm_query_config(4096, 4096, 4096)
+    assert cfg["grid"] > 0 and cfg["tiles"] == (4096 // cfg["bm"]) * (4096 // cfg["bn"])
+    assert cfg["ctas_per_sm"] >= 1
+    rag = sgemm_query_config(3001, 2047, 1999)
+    assert rag["vec"] == 1   # odd leading dimensions: 4-byte loads
+
+
+def test_launch_counter_counts(cuda):
+    torch = cuda
+    from dense_fp32_gemm_09_gb300 import launch_count
+    A = torch.ones(64, 64, device="cuda")
+    n0 = launch_count()
+    sgemm(A, A)
+    assert launch_count() == n0 + 1
