@@ -12,6 +12,7 @@ from ._abi import (SGEMM_ERR_INVALID_ARG, SGEMM_ERR_LAUNCH, SGEMM_ERR_UNSUPPORTE
                    SGEMM_ERR_WORKSPACE, SGEMM_OK, SgemmConfig, SgemmError, check, load)
 
 __all__ = ["sgemm", "sgemm_run", "sgemm_run_ws", "sgemm_run_with", "sgemm_run_host",
+           "sgemm_run_noalloc",
            "sgemm_query_config", "sgemm_workspace_size", "kernel_table", "launch_count",
            "SgemmError", "load"]
 
@@ -52,6 +53,13 @@ def sgemm_run_ws(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, ws_ptr, ws_bytes,
                  stream=None) -> int:
     return load().sgemm_run_ws(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, ws_ptr, ws_bytes,
                                _stream_handle(stream))
+
+
+def sgemm_run_noalloc(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, stream=None) -> int:
+    """Raw call of ``sgemm_run_noalloc``: like ``sgemm_run`` but the library allocates
+    no device memory (split-tile scratch comes from a fixed static array)."""
+    return load().sgemm_run_noalloc(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc,
+                                    _stream_handle(stream))
 
 
 def sgemm_run_with(M, N, K, A_ptr, lda, B_ptr, ldb, C_ptr, ldc, kernel_id, schedule=0,

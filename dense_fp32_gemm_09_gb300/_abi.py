@@ -37,6 +37,7 @@ _RUN = [_i, _i, _i, _vp, _i, _vp, _i, _vp, _i]
 SIGNATURES = {
     "sgemm_run": (_i, _RUN + [_vp]),
     "sgemm_run_ws": (_i, _RUN + [_vp, _sz, _vp]),
+    "sgemm_run_noalloc": (_i, _RUN + [_vp]),
     "sgemm_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                                   ctypes.POINTER(_sz)]),
     "sgemm_run_with": (_i, _RUN + [_i, _i, _vp]),

@@ -477,6 +477,11 @@ int check_schedule(const Plan& p, char* why, size_t why_len) {
 }
 
 }  // namespace
+
+void set_last_error_message(const char* msg) {
+    std::snprintf(t_last_error, sizeof(t_last_error), "%s", msg);
+}
+
 }  // namespace sgemm
 
 using namespace sgemm;

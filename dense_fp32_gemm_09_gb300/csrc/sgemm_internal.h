@@ -43,4 +43,7 @@ struct KernelEntry {
 cudaError_t launch_sk_reduce(const GemmArgs& a, int bm, int bn, int sms, cudaStream_t stream);
 int reduce_chunks(int bm, int bn, int sk_tiles, int sms);
 
+// Sets the text sgemm_last_error() returns on this thread.
+void set_last_error_message(const char* msg);
+
 }  // namespace sgemm

@@ -102,6 +102,29 @@ SGEMM_API int sgemm_run(int M, int N, int K, const float* A, int lda, const floa
 SGEMM_API int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                  float* C, int ldc, void* ws, size_t ws_bytes, sgemm_stream_t stream);
 
+/* Size of the static scratch array sgemm_run_noalloc uses (40 MiB). */
+#define SGEMM_NOALLOC_SCRATCH_BYTES (40u << 20)
+
+/* As sgemm_run, but the library allocates no device memory at all; for callers
+ * that cannot let a library call cudaMalloc (it can synchronise the device and
+ * take unbounded time on a latency-critical path, and some processes reserve
+ * their whole device memory budget up front).  The source pages have no
+ * counterpart to this entry point: it exists only for such callers.
+ *
+ * When the schedule splits tiles between CTAs, the partial tiles go to one
+ * static __device__ array of SGEMM_NOALLOC_SCRATCH_BYTES compiled into the
+ * library; every GPU that loads the library holds that array until the process
+ * exits.  A problem that would need more scratch than that is rejected with
+ * SGEMM_ERR_WORKSPACE and a message in sgemm_last_error(); nothing is launched.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture begins.  All
+ * calls on a device share the array, so calls that can overlap on the GPU
+ * (e.g. on different streams without ordering between them) race and must not
+ * be issued; calls ordered on one stream are fine.  A, B, C and `stream` are as
+ * for sgemm_run. */
+SGEMM_API int sgemm_run_noalloc(int M, int N, int K, const float* A, int lda, const float* B,
+                                int ldb, float* C, int ldc, sgemm_stream_t stream);
+
 /* Bytes of workspace sgemm_run_ws needs for these arguments (0 if none). */
 SGEMM_API int sgemm_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
                          const float* A, const float* B, const float* C, size_t* out_bytes);
