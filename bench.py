@@ -67,6 +67,25 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over all ranks of the default process group
+    (identity when not distributed).  The timed region's length is the slowest
+    rank's, so throughput is computed from these maxima."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Aggregate throughput of `world` replicas that each did `flops_per_rank` in a
+    region whose (max over ranks) length is `ms`."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def measured_peaks() -> dict:
     try:
         with open(os.path.join(REPO, "MEASURED_PEAKS.json")) as f:
@@ -229,7 +248,16 @@ def bench_gpu(args, w, dist_ctx):
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    run_args = (w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N, dC.data_ptr(), w.N, sh)
+    scaled = args.alpha != 1.0 or args.beta != 0.0
+    if scaled:
+        dC.normal_()
+        run_fn = lib.sgemm_run_ex
+        run_args = (w.M, w.N, w.K, args.alpha, dA.data_ptr(), w.K, dB.data_ptr(), w.N, args.beta,
+                    dC.data_ptr(), w.N, -1, 0, sh)
+    else:
+        run_fn = lib.sgemm_run
+        run_args = (w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N, dC.data_ptr(), w.N,
+                    sh)
     cfg = sg.sgemm_query_config(w.M, w.N, w.K, w.K, w.N, w.N, dA.data_ptr(), dB.data_ptr(),
                                 dC.data_ptr())
 
@@ -241,7 +269,7 @@ def bench_gpu(args, w, dist_ctx):
 
     for _ in range(args.warmup):
         flush.fill_(1.0)
-        check(lib.sgemm_run(*run_args), "sgemm_run")
+        check(run_fn(*run_args), "sgemm_run")
     barrier()
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -253,7 +281,7 @@ def bench_gpu(args, w, dist_ctx):
         for i in range(args.steps):
             flush.fill_(float(i))
             starts[i].record(stream)
-            check(lib.sgemm_run(*run_args), "sgemm_run")
+            check(run_fn(*run_args), "sgemm_run")
             ends[i].record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
@@ -261,11 +289,7 @@ def bench_gpu(args, w, dist_ctx):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     med_ms = statistics.median(step_ms)
     mean_ms = statistics.fmean(step_ms)
-    if world > 1:
-        import torch.distributed as tdist
-        t = torch.tensor([med_ms, mean_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        med_ms, mean_ms = (float(x) for x in t.tolist())
+    med_ms, mean_ms = max_over_ranks([med_ms, mean_ms], dev)
 
     # end to end through the host-buffer entry point: pinned host in, pinned host out
     hA, hB = A.pin_memory(), B.pin_memory()
@@ -283,11 +307,7 @@ def bench_gpu(args, w, dist_ctx):
     ee.record(stream)
     barrier()
     e2e_ms = es.elapsed_time(ee) / e2e_steps
-    if world > 1:
-        import torch.distributed as tdist
-        t = torch.tensor([e2e_ms], device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev)
 
     if rank != 0:
         return None
@@ -297,7 +317,7 @@ def bench_gpu(args, w, dist_ctx):
     max_mhz = float(peaks.get("sm_max_mhz") or clocks.summary().get("sm_max_mhz") or 2070.0)
     peak_tflops = sms * FMA_PER_CLK_PER_SM * 2 * max_mhz * 1e6 / 1e12
     flops = float(w.flops)
-    value = world * flops / (med_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, med_ms)
     achieved = flops / (med_ms * 1e-3) / 1e12
     clk = clocks.summary()
     line = {
@@ -306,7 +326,9 @@ def bench_gpu(args, w, dist_ctx):
         "ms_per_step_mean": mean_ms, "wall_s_timed_region": t_wall,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
+        "config": {"workload": describe(w) + (f"; C = {args.alpha:g}*A.B + {args.beta:g}*C"
+                                              if scaled else ""),
+                   "M": w.M, "N": w.N, "K": w.K,
                    "l2": "flushed before every step (256 MiB write, outside the events)",
                    "kernel": cfg["name"], "grid": cfg["grid"], "tiles": cfg["tiles"],
                    "sk_tiles": cfg["sk_tiles"], "ctas_per_sm": cfg["ctas_per_sm"],
@@ -321,7 +343,7 @@ def bench_gpu(args, w, dist_ctx):
                          achieved / (sms * FMA_PER_CLK_PER_SM * 2 * clk["sm_mhz"] * 1e-6)
                          if clk.get("sm_mhz") else None)},
         "clocks": clk,
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
                 "d2h_bytes_per_step": 4 * w.M * w.N},
@@ -339,6 +361,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--sweep", action="store_true", help="one line per named workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--alpha", type=float, default=1.0, help="C = alpha*A.B + beta*C")
+    ap.add_argument("--beta", type=float, default=0.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -12,7 +12,7 @@ from ._abi import (SGEMM_ERR_INVALID_ARG, SGEMM_ERR_LAUNCH, SGEMM_ERR_UNSUPPORTE
                    SGEMM_ERR_WORKSPACE, SGEMM_OK, SgemmConfig, SgemmError, check, load)
 
 __all__ = ["sgemm", "sgemm_run", "sgemm_run_ws", "sgemm_run_with", "sgemm_run_host",
-           "sgemm_run_noalloc",
+           "sgemm_run_noalloc", "sgemm_run_ex",
            "sgemm_query_config", "sgemm_workspace_size", "kernel_table", "launch_count",
            "SgemmError", "load"]
 
@@ -106,11 +106,21 @@ def launch_count() -> int:
     return int(load().sgemm_launch_count())
 
 
-def sgemm(A, B, out=None, *, kernel_id: int | None = None, schedule: int = 0, stream=None):
-    """C = A @ B for float32 CUDA tensors (row-major views with unit column stride).
+def sgemm_run_ex(M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, kernel_id=-1,
+                 schedule=0, stream=None) -> int:
+    """Raw call of ``sgemm_run_ex``: C = alpha * A.B + beta * C."""
+    return load().sgemm_run_ex(M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
+                               kernel_id, schedule, _stream_handle(stream))
 
-    ``out`` may be a preallocated (M, N) float32 CUDA view; it is overwritten.
-    ``kernel_id``/``schedule`` force a tile-table entry (tests and tuning)."""
+
+def sgemm(A, B, out=None, *, alpha: float = 1.0, beta: float = 0.0,
+          kernel_id: int | None = None, schedule: int = 0, stream=None):
+    """C = alpha * A @ B + beta * C for float32 CUDA tensors (row-major views with
+    unit column stride).
+
+    ``out`` may be a preallocated (M, N) float32 CUDA view; with beta == 0 it is
+    only written, otherwise its contents are the C of the formula (beta != 0
+    needs ``out``).  ``kernel_id``/``schedule`` force a tile-table entry."""
     import torch
     _check_operand(A, "A")
     _check_operand(B, "B")
@@ -119,6 +129,8 @@ def sgemm(A, B, out=None, *, kernel_id: int | None = None, schedule: int = 0, st
     if K != K2:
         raise ValueError(f"inner dimensions differ: A is {tuple(A.shape)}, B is {tuple(B.shape)}")
     if out is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs `out` (the C that is scaled)")
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     else:
         _check_operand(out, "out")
@@ -129,7 +141,12 @@ def sgemm(A, B, out=None, *, kernel_id: int | None = None, schedule: int = 0, st
     lda, ldb, ldc = _ld(A, "A"), _ld(B, "B"), _ld(out, "out")
     args = (M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc)
     with torch.cuda.device(A.device):
-        if kernel_id is None and schedule == 0:
+        if alpha != 1.0 or beta != 0.0:
+            st = sgemm_run_ex(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                              float(beta), out.data_ptr(), ldc,
+                              -1 if kernel_id is None else kernel_id, schedule, stream=stream)
+            check(st, "sgemm_run_ex")
+        elif kernel_id is None and schedule == 0:
             st = sgemm_run(*args, stream=stream)
             check(st, "sgemm_run")
         else:

@@ -297,25 +297,30 @@ int library_workspace(cudaStream_t stream, size_t need, void** out) {
     return SGEMM_OK;
 }
 
-__global__ void zero_fill_kernel(float* C, int M, int N, long long ldc) {
+// C = beta * C over the M x N region (beta == 0 writes zeros without reading C):
+// the whole product when K == 0 (the empty sum) or alpha == 0.
+__global__ void scale_c_kernel(float* C, int M, int N, long long ldc, float beta) {
     const long long total = static_cast<long long>(M) * N;
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
         const long long i = e / N, j = e - i * N;
-        C[i * ldc + j] = 0.0f;
+        float* c = C + i * ldc + j;
+        *c = beta == 0.0f ? 0.0f : beta * *c;
     }
 }
 
-int launch_zero(float* C, int M, int N, int ldc, cudaStream_t stream, const DeviceInfo* d) {
+int launch_scale(float* C, int M, int N, int ldc, float beta, cudaStream_t stream,
+                 const DeviceInfo* d) {
+    if (beta == 1.0f) return SGEMM_OK;
     const long long total = static_cast<long long>(M) * N;
     const int threads = 256;
     const long long blocks =
         std::min<long long>((total + threads - 1) / threads, static_cast<long long>(d->sms) * 8);
-    zero_fill_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(C, M, N, ldc);
+    scale_c_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(C, M, N, ldc, beta);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
-        set_error("zero_fill_kernel launch", e);
+        set_error("scale_c_kernel launch", e);
         return SGEMM_ERR_LAUNCH;
     }
     return SGEMM_OK;
@@ -352,15 +357,17 @@ int launch(const Plan& p, cudaStream_t stream) {
 
 // Common body of the run entry points.  ws == nullptr with ws_bytes == SIZE_MAX
 // means "use the library-owned workspace".
-int run_impl(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
-             int ldc, int forced_entry, int schedule, void* ws, size_t ws_bytes,
-             bool library_ws, cudaStream_t stream) {
+// C = alpha * A.B + beta * C; the plain entry points pass alpha = 1, beta = 0.
+int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
+             float beta, float* C, int ldc, int forced_entry, int schedule, void* ws,
+             size_t ws_bytes, bool library_ws, cudaStream_t stream) {
     int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (M == 0 || N == 0) return SGEMM_OK;
     Plan p;
     const DeviceInfo* d = nullptr;
-    if (K == 0) {
+    if (K == 0 || alpha == 0.0f) {
+        // The product term vanishes (empty sum, or alpha = 0): A and B are not read.
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess) {
@@ -369,10 +376,13 @@ int run_impl(int M, int N, int K, const float* A, int lda, const float* B, int l
         }
         rc = device_info(dev, &d);
         if (rc != SGEMM_OK) return rc;
-        return launch_zero(C, M, N, ldc, stream, d);
+        return launch_scale(C, M, N, ldc, beta, stream, d);
     }
     rc = plan(M, N, K, A, lda, B, ldb, C, ldc, forced_entry, schedule, p, &d);
     if (rc != SGEMM_OK) return rc;
+    p.args.alpha = alpha;
+    p.args.beta = beta;
+    p.args.epi = (beta != 0.0f) ? kEpiAlphaBeta : (alpha != 1.0f ? kEpiAlpha : kEpiPlain);
     const size_t need = p.ws_partial_bytes;
     if (need > 0) {
         void* base = nullptr;
@@ -490,13 +500,29 @@ extern "C" {
 
 int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb, float* C,
               int ldc, sgemm_stream_t stream) {
-    return run_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, 0, nullptr, 0, true,
+    return run_impl(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, -1, 0, nullptr, 0, true,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sgemm_run_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
+                 int ldb, float beta, float* C, int ldc, int kernel_id, int schedule,
+                 sgemm_stream_t stream) {
+    if (kernel_id < -1 || schedule < 0 || schedule > 2) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "bad kernel_id %d or schedule %d",
+                      kernel_id, schedule);
+        return kernel_id < -1 ? SGEMM_ERR_UNSUPPORTED : SGEMM_ERR_INVALID_ARG;
+    }
+    if (!(alpha == alpha) || !(beta == beta)) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "alpha or beta is NaN");
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    return run_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, kernel_id, schedule, nullptr,
+                    0, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                  float* C, int ldc, void* ws, size_t ws_bytes, sgemm_stream_t stream) {
-    return run_impl(M, N, K, A, lda, B, ldb, C, ldc, -1, 0, ws, ws_bytes, false,
+    return run_impl(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, -1, 0, ws, ws_bytes, false,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -507,7 +533,8 @@ int sgemm_run_with(int M, int N, int K, const float* A, int lda, const float* B,
                       kernel_id, schedule);
         return kernel_id < -1 ? SGEMM_ERR_UNSUPPORTED : SGEMM_ERR_INVALID_ARG;
     }
-    return run_impl(M, N, K, A, lda, B, ldb, C, ldc, kernel_id, schedule, nullptr, 0, true,
+    return run_impl(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, kernel_id, schedule, nullptr, 0,
+                    true,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -36,6 +36,7 @@
 
 #include <stdint.h>
 
+#include "sgemm_epilogue.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_sched.cuh"
 
@@ -292,18 +293,8 @@ __device__ __forceinline__ void store_tile(const GemmArgs& a, const AccT& acc, i
         if (gm >= a.M) continue;
         float* crow = a.C + gm * a.ldc;
 #pragma unroll
-        for (int j4 = 0; j4 < TN / 4; ++j4) {
-            const int gn = n0 + b_col0 + j4 * LC * 4;
-            const float4 v = acc.chunk(i, j4);
-            if (a.c_vec && gn + 3 < a.N) {
-                *reinterpret_cast<float4*>(crow + gn) = v;
-            } else {
-                if (gn + 0 < a.N) crow[gn + 0] = v.x;
-                if (gn + 1 < a.N) crow[gn + 1] = v.y;
-                if (gn + 2 < a.N) crow[gn + 2] = v.z;
-                if (gn + 3 < a.N) crow[gn + 3] = v.w;
-            }
-        }
+        for (int j4 = 0; j4 < TN / 4; ++j4)
+            store_c4(a, crow, n0 + b_col0 + j4 * LC * 4, acc.chunk(i, j4));
     }
 }
 
@@ -408,6 +399,9 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const Ge
         }
     }
     cp_async_wait<0>();
+    // Lets a programmatic dependent launch (the stream-K reduction) get scheduled
+    // now; it still waits for this whole grid to finish before reading results.
+    asm volatile("griddepcontrol.launch_dependents;");
 }
 
 template <class Cfg>

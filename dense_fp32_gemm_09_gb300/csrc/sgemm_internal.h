@@ -8,6 +8,8 @@
 
 namespace sgemm {
 
+enum : int { kEpiPlain = 0, kEpiAlpha = 1, kEpiAlphaBeta = 2 };
+
 // Everything one launch needs, passed by value in the kernel parameter space.
 struct GemmArgs {
     int M, N, K;
@@ -16,6 +18,8 @@ struct GemmArgs {
     float* C;
     long long lda, ldb, ldc;
     int c_vec;            // 1: C and ldc allow 16-byte stores
+    int epi;              // kEpiPlain (C = acc), kEpiAlpha, kEpiAlphaBeta
+    float alpha, beta;    // C = alpha * A.B + beta * C (beta == 0: C is not read)
 
     // Tile grid and schedule (see the persistent scheduler in sgemm_ffma.cuh).
     int tiles_m, tiles_n;  // ceil(M/BM), ceil(N/BN)

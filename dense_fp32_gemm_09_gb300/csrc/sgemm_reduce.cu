@@ -7,6 +7,7 @@
 // CTA order, i.e. in increasing k, which fixes the summation order: the result
 // does not depend on timing.  The schedule formulas are the ones the main
 // kernel used (sgemm_sched.cuh).
+#include "sgemm_epilogue.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_sched.cuh"
 
@@ -20,6 +21,9 @@ constexpr int kBatch = 8;
 __global__ void __launch_bounds__(kReduceThreads) sk_reduce_kernel(const GemmArgs a, int bm,
                                                                    int bn, int chunks) {
     __shared__ const float4* s_src[kMaxSplit];
+    // Launched as a programmatic dependent of the main kernel: everything above
+    // this wait overlaps the main kernel's tail; nothing it wrote is read before.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.x / chunks, part = blockIdx.x - t * chunks;
     const long long tb = static_cast<long long>(t) * a.KT;
     const int g0 = sk_owner(tb, a.grid, a.sk_iters);
@@ -60,15 +64,7 @@ __global__ void __launch_bounds__(kReduceThreads) sk_reduce_kernel(const GemmArg
         const int r = (4 * e) / bn, c = (4 * e) - r * bn;
         const int gm = m0 + r, gn = n0 + c;
         if (gm >= a.M) continue;
-        float* crow = a.C + gm * a.ldc;
-        if (a.c_vec && gn + 3 < a.N) {
-            *reinterpret_cast<float4*>(crow + gn) = s;
-        } else {
-            if (gn + 0 < a.N) crow[gn + 0] = s.x;
-            if (gn + 1 < a.N) crow[gn + 1] = s.y;
-            if (gn + 2 < a.N) crow[gn + 2] = s.z;
-            if (gn + 3 < a.N) crow[gn + 3] = s.w;
-        }
+        store_c4(a, a.C + gm * a.ldc, gn, s);
     }
 }
 
@@ -83,10 +79,25 @@ int reduce_chunks(int bm, int bn, int sk_tiles, int sms) {
 }
 
 cudaError_t launch_sk_reduce(const GemmArgs& a, int bm, int bn, int sms, cudaStream_t stream) {
-    const int chunks = reduce_chunks(bm, bn, a.sk_tiles, sms);
-    sk_reduce_kernel<<<static_cast<unsigned>(a.sk_tiles) * chunks, kReduceThreads, 0, stream>>>(
-        a, bm, bn, chunks);
-    return cudaGetLastError();
+    int chunks = reduce_chunks(bm, bn, a.sk_tiles, sms);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.sk_tiles) * chunks);
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    // Programmatic dependent launch: the reduction is scheduled as the main
+    // kernel's CTAs finish and waits (griddepcontrol.wait) for its completion.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    GemmArgs args = a;
+    void* params[] = {&args, &bm, &bn, &chunks};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(&sk_reduce_kernel),
+                                        params);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e;
 }
 
 }  // namespace sgemm

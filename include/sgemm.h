@@ -93,6 +93,19 @@ typedef struct {
 SGEMM_API int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
               float* C, int ldc, sgemm_stream_t stream);
 
+/* Scaled form: C = alpha * A.B + beta * C, with the BLAS conventions: when
+ * beta == 0, C is only written (its old contents, NaN included, are ignored);
+ * when alpha == 0 or K == 0, A and B are not read and C = beta * C.  The plain
+ * entry points are this with alpha = 1, beta = 0.  ("기존 작성한 GE_v2 의 regemm
+ * 타일드 커널의 1:1 매핑, gemm_tiled_test 작성" names the GE_v2 kernel's epilogue,
+ * which its test kernel removes; the scaling rule itself is the BLAS one.)
+ * The scaled value is fmaf(alpha, acc, beta * c) per element.  kernel_id = -1 and
+ * schedule = 0 select automatically; other values force a tile-table entry and
+ * schedule as for sgemm_run_with.  alpha or beta NaN -> SGEMM_ERR_INVALID_ARG. */
+SGEMM_API int sgemm_run_ex(int M, int N, int K, float alpha, const float* A, int lda,
+                           const float* B, int ldb, float beta, float* C, int ldc,
+                           int kernel_id, int schedule, sgemm_stream_t stream);
+
 /* As sgemm_run, with a caller-owned device workspace of `ws_bytes` bytes (at least
  * sgemm_workspace_size() for the same arguments, 16-byte aligned; may be NULL
  * when that size is 0).  The library allocates nothing on this path.  The

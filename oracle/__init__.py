@@ -56,7 +56,10 @@ def _load():
         lib.oracle_gemm_f64_elems.argtypes = [i, i, i, f32p, i64, f32p, i64, i32p, i32p, i,
                                               f64p]
         lib.oracle_gemm_f32_fma_seq.argtypes = [i, i, i, f32p, i64, f32p, i64, f32p, i64]
-        for fn in (lib.oracle_gemm_f64, lib.oracle_gemm_f64_rows,
+        d = ctypes.c_double
+        lib.oracle_gemm_f64_ex.argtypes = [i, i, i, d, f32p, i64, f32p, i64, d, f32p, i64,
+                                           i32p, i, f64p, i]
+        for fn in (lib.oracle_gemm_f64, lib.oracle_gemm_f64_rows, lib.oracle_gemm_f64_ex,
                    lib.oracle_gemm_f64_elems, lib.oracle_gemm_f32_fma_seq,
                    lib.oracle_max_threads):
             fn.restype = ctypes.c_int
@@ -143,6 +146,40 @@ def gemm_f64_elems(A, B, ii, jj) -> np.ndarray:
                                        ii.size, _ptr(out, ctypes.c_double))
     if rc != 0:
         raise ValueError("oracle_gemm_f64_elems rejected its arguments")
+    return out
+
+
+def gemm_f64_ex(alpha, A, B, beta, C0, rows=None, nthreads: int | None = None) -> np.ndarray:
+    """alpha * (A.B) + beta * C0 in double (BLAS conventions: beta == 0 does not
+    read C0, alpha == 0 does not read A or B).  With `rows`, only those rows of the
+    result are returned.  C0 may be None when beta == 0."""
+    A, lda = _mat(A, "A")
+    B, ldb = _mat(B, "B")
+    M, K = A.shape
+    N = B.shape[1]
+    if B.shape[0] != K:
+        raise ValueError("inner dimensions differ")
+    if C0 is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C0")
+        C0 = np.zeros((1, max(N, 1)), dtype=np.float32)
+        ldc0 = max(N, 1)
+    else:
+        C0, ldc0 = _mat(C0, "C0")
+        if C0.shape != (M, N):
+            raise ValueError("C0 must be M x N")
+    if rows is None:
+        rp, nrows = None, M
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int32)
+        rp, nrows = _ptr(rows, ctypes.c_int32), rows.size
+    out = np.empty((nrows, N), dtype=np.float64)
+    rc = _load().oracle_gemm_f64_ex(M, N, K, float(alpha), _ptr(A, ctypes.c_float), lda,
+                                    _ptr(B, ctypes.c_float), ldb, float(beta),
+                                    _ptr(C0, ctypes.c_float), ldc0, rp, nrows,
+                                    _ptr(out, ctypes.c_double), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_gemm_f64_ex rejected its arguments")
     return out
 
 

@@ -130,6 +130,42 @@ int oracle_gemm_f32_fma_seq(int M, int N, int K, const float* A, int64_t lda,
     return 0;
 }
 
+/* Scaled form, in double:  out[r][j] = alpha * C[i][j] + beta * C0[i][j]  with
+ * C[i][j] the product above and i = rows[r] (rows == NULL: i = r for all M rows).
+ * BLAS conventions: beta == 0 -> C0 is not read; alpha == 0 -> A and B are not
+ * read.  ("기존 작성한 GE_v2 의 regemm 타일드 커널의 1:1 매핑, gemm_tiled_test 작성"
+ * names the GE_v2 epilogue that its test kernel strips; this is the usual
+ * alpha/beta reading of it.)  out is nrows x N with leading dimension N. */
+int oracle_gemm_f64_ex(int M, int N, int K, double alpha, const float* A, int64_t lda,
+                       const float* B, int64_t ldb, double beta, const float* C0,
+                       int64_t ldc0, const int32_t* rows, int nrows, double* out,
+                       int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (rows == NULL && nrows != M) return -1;
+    if (lda < (K > 0 ? K : 1) || ldb < (N > 0 ? N : 1) || ldc0 < (N > 0 ? N : 1)) return -1;
+    if (nrows > 0 && N > 0 && out == NULL) return -1;
+    if (alpha != 0.0 && K > 0 && nrows > 0 && N > 0 && (A == NULL || B == NULL)) return -1;
+    if (beta != 0.0 && nrows > 0 && N > 0 && C0 == NULL) return -1;
+    for (int r = 0; r < nrows; ++r)
+        if (rows != NULL && (rows[r] < 0 || rows[r] >= M)) return -1;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int r = 0; r < nrows; ++r) {
+        const int i = rows != NULL ? rows[r] : r;
+        double* o = out + (int64_t)r * N;
+        if (alpha != 0.0) {
+            one_row_f64(N, K, A + (int64_t)i * lda, B, ldb, o);
+            for (int j = 0; j < N; ++j) o[j] *= alpha;
+        } else {
+            for (int j = 0; j < N; ++j) o[j] = 0.0;
+        }
+        if (beta != 0.0)
+            for (int j = 0; j < N; ++j) o[j] += beta * (double)C0[(int64_t)i * ldc0 + j];
+    }
+    return 0;
+}
+
 /* Threads an OpenMP region would use here (for reporting the CPU baseline). */
 int oracle_max_threads(void)
 {

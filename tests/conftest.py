@@ -48,3 +48,15 @@ def cuda():
     from dense_fp32_gemm_09_gb300 import build
     build.build()
     return torch
+
+
+def padded_device(torch, X, pad, offset=0):
+    """X copied into a device buffer with leading dimension cols + pad, starting
+    `offset` elements into the buffer (offset 1 breaks 16-byte alignment)."""
+    rows, cols = X.shape
+    ld = cols + pad
+    flat = torch.full((offset + rows * ld + 8,), float("nan"), dtype=torch.float32,
+                      device="cuda")
+    view = flat[offset:offset + rows * ld].view(rows, ld)[:, :cols]
+    view.copy_(X)
+    return view

@@ -266,3 +266,54 @@ def test_random_shapes_against_numpy_float64(oracle_mod):
         want = A.astype(np.float64) @ B.astype(np.float64)
         scale = np.abs(A.astype(np.float64)) @ np.abs(B.astype(np.float64))
         assert np.all(np.abs(oracle_mod.gemm_f64(A, B) - want) <= 1e-13 * scale + 1e-300)
+
+
+# --------------------------------------------------------------------------
+# scaled form: alpha * A.B + beta * C0
+# --------------------------------------------------------------------------
+
+
+def test_ex_small_integers_exact(oracle_mod):
+    rng = np.random.default_rng(21)
+    A = rng.integers(-8, 9, (23, 301)).astype(np.float32)
+    B = rng.integers(-8, 9, (301, 17)).astype(np.float32)
+    C0 = rng.integers(-100, 101, (23, 17)).astype(np.float32)
+    want = 2 * (A.astype(np.int64) @ B.astype(np.int64)) - 3 * C0.astype(np.int64)
+    assert np.array_equal(oracle_mod.gemm_f64_ex(2.0, A, B, -3.0, C0), want.astype(np.float64))
+    rows = np.array([22, 0, 5], dtype=np.int32)
+    assert np.array_equal(oracle_mod.gemm_f64_ex(2.0, A, B, -3.0, C0, rows=rows),
+                          want[rows].astype(np.float64))
+
+
+def test_ex_beta_zero_does_not_read_C(oracle_mod):
+    rng = np.random.default_rng(22)
+    A = rng.integers(-4, 5, (9, 40)).astype(np.float32)
+    B = rng.integers(-4, 5, (40, 11)).astype(np.float32)
+    C0 = np.full((9, 11), np.nan, dtype=np.float32)
+    want = 0.5 * (A.astype(np.int64) @ B.astype(np.int64))
+    assert np.array_equal(oracle_mod.gemm_f64_ex(0.5, A, B, 0.0, C0), want)
+
+
+def test_ex_alpha_zero_does_not_read_A_or_B(oracle_mod):
+    A = np.full((6, 5), np.nan, dtype=np.float32)
+    B = np.full((5, 7), np.inf, dtype=np.float32)
+    C0 = np.arange(42, dtype=np.float32).reshape(6, 7)
+    assert np.array_equal(oracle_mod.gemm_f64_ex(0.0, A, B, 0.25, C0), 0.25 * C0.astype(np.float64))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_ex_against_exact_rationals(oracle_mod, seed):
+    rng = np.random.default_rng(300 + seed)
+    M, N, K = (int(x) for x in rng.integers(1, 7, size=3))
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    C0 = rng.standard_normal((M, N)).astype(np.float32)
+    alpha, beta = float(np.float32(0.1)), float(np.float32(-0.3))
+    got = oracle_mod.gemm_f64_ex(alpha, A, B, beta, C0)
+    exact, absum = exact_product(A, B)
+    u = 2.0 ** -53
+    for i in range(M):
+        for j in range(N):
+            want = Fraction(alpha) * exact[i][j] + Fraction(beta) * Fraction(float(C0[i, j]))
+            bound = (K + 3) * u * (abs(alpha) * float(absum[i][j]) + abs(beta * float(C0[i, j])))
+            assert abs(got[i, j] - float(want)) <= 1.01 * bound + 1e-300

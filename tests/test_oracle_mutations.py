@@ -27,6 +27,8 @@ MUTATIONS = {
                       "crow[j] += a * (double)B[(int64_t)j * ldb + k];")],
     "ignores_lda": [("one_row_f64(N, K, A + (int64_t)i * lda,",
                      "one_row_f64(N, K, A + (int64_t)i * K,")],
+    "drops_beta_term": [("o[j] += beta * (double)C0[(int64_t)i * ldc0 + j];",
+                         "o[j] += 0.0 * (double)C0[(int64_t)i * ldc0 + j];")],
     "unfused_fp32": [("acc = fmaf(A[(int64_t)i * lda + k], B[(int64_t)k * ldb + j], acc);",
                       "acc = A[(int64_t)i * lda + k] * B[(int64_t)k * ldb + j] + acc;")],
 }
@@ -47,6 +49,8 @@ def build_variant(tmp_path, name):
     i, i64 = ctypes.c_int, ctypes.c_int64
     lib.oracle_gemm_f64.argtypes = [i, i, i, f32p, i64, f32p, i64, f64p, i64, i]
     lib.oracle_gemm_f32_fma_seq.argtypes = [i, i, i, f32p, i64, f32p, i64, f32p, i64]
+    lib.oracle_gemm_f64_ex.argtypes = [i, i, i, ctypes.c_double, f32p, i64, f32p, i64,
+                                       ctypes.c_double, f32p, i64, ctypes.c_void_p, i, f64p, i]
     return lib
 
 
@@ -84,6 +88,15 @@ def failing_pins(lib):
     want = (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64)
     if not np.array_equal(call_f64(lib, A, n, B, n, n, n, n), want):
         fails.append("small_integers")
+    # scaled form: alpha * A.B + beta * C0 on small integers
+    C0 = rng.integers(-50, 51, (n, n)).astype(np.float32)
+    out = np.empty((n, n), dtype=np.float64)
+    lib.oracle_gemm_f64_ex(n, n, n, 2.0, A.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), n,
+                           B.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), n, -3.0,
+                           C0.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), n, None, n,
+                           out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), 1)
+    if not np.array_equal(out, 2 * want - 3 * C0.astype(np.float64)):
+        fails.append("scaled_small_integers")
     # the pages' printed worked example (fp32 mode)
     rows = {r[0]: r[1:] for r in read_golden("p1_micro_gemm_4x4.txt")}
     K = int(rows["K"][0])
