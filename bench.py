@@ -352,6 +352,112 @@ def bench_gpu(args, w, dist_ctx):
     return line
 
 
+TF32_PER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor rates of the GB300
+
+
+def bench_tf32x3(args, w, dist_ctx):
+    """The 3xTF32 tensor-core variant: one step = operand split + tcgen05 GEMM."""
+    import ctypes as ct
+
+    import torch
+
+    import dense_fp32_gemm_09_gb300 as sg
+    from dense_fp32_gemm_09_gb300._abi import check
+
+    rank, world, local = dist_ctx
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = sg.load()
+    A, B = make_inputs(w)
+    dA, dB = A.to(dev), B.to(dev)
+    dC = torch.empty(w.M, w.N, device=dev)
+    need = ct.c_size_t(0)
+    check(lib.sgemm_tf32x3_workspace_size(w.M, w.N, w.K, ct.byref(need)), "workspace size")
+    ws = torch.empty(need.value // 4 + 64, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    prep = (w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N, ws.data_ptr(), need.value, sh)
+    mult = (w.M, w.N, w.K, args.alpha, args.beta, dC.data_ptr(), w.N, ws.data_ptr(), need.value,
+            sh)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        check(lib.sgemm_tf32x3_prepare(*prep), "prepare")
+        check(lib.sgemm_tf32x3_multiply(*mult), "multiply")
+    barrier()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    n0 = lib.sgemm_launch_count()
+    with ClockSampler(local) as clocks:
+        barrier()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            check(lib.sgemm_tf32x3_prepare(*prep), "prepare")
+            ev[i][1].record(stream)
+            check(lib.sgemm_tf32x3_multiply(*mult), "multiply")
+            ev[i][2].record(stream)
+        barrier()
+    launches = lib.sgemm_launch_count() - n0
+    check(lib.sgemm_device_status(), "device status")
+    step_ms = statistics.median(e[0].elapsed_time(e[2]) for e in ev)
+    split_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    gemm_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms, split_ms, gemm_ms = max_over_ranks([step_ms, split_ms, gemm_ms], dev)
+
+    # end to end: pinned host in, pinned host out, through the public entry point
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.empty(w.M, w.N).pin_memory()
+    run_ex = (w.M, w.N, w.K, 1.0, dA.data_ptr(), w.K, dB.data_ptr(), w.N, 0.0, dC.data_ptr(),
+              w.N, ws.data_ptr(), need.value, sh)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    es.record(stream)
+    for _ in range(e2e_steps):
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        check(lib.sgemm_tf32x3_run_ex(*run_ex), "run_ex")
+        hC.copy_(dC, non_blocking=True)
+    ee.record(stream)
+    barrier()
+    (e2e_ms,) = max_over_ranks([es.elapsed_time(ee) / e2e_steps], dev)
+    if rank != 0:
+        return None
+    peaks = measured_peaks()
+    bf16 = float(peaks.get("bf16_tflops") or 1900.0)
+    peak = bf16 * TF32_PER_BF16
+    flops = float(w.flops)
+    clk = clocks.summary()
+    return {
+        "metric": METRIC, "path": "tf32x3", "value": whole_job_tflops(world, flops, step_ms),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_ms, "ms_split": split_ms, "ms_gemm": gemm_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32x3",
+        "data": "synthetic",
+        "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
+                   "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "kernel": "tf32x3_kernel<BN=256, 2 stages> + split kernels",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": {"bound": "tensor", "achieved": 3 * flops / (gemm_ms * 1e-3) / 1e12,
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": 3 * flops / (gemm_ms * 1e-3) / 1e12 / peak, "traffic": None,
+                     "peak_basis": f"measured bf16 {bf16:.1f} TFLOP/s x nominal TF32/BF16 "
+                                   f"ratio {TF32_PER_BF16:.3f}; 3 TF32 MMAs per product",
+                     "effective_fp32_tflops_gemm_only": flops / (gemm_ms * 1e-3) / 1e12},
+        "clocks": clk,
+        "e2e": {"value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
+                "d2h_bytes_per_step": 4 * w.M * w.N},
+        "gpu_launches": int(launches),
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -361,6 +467,9 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--sweep", action="store_true", help="one line per named workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["ffma", "tf32x3"], default="ffma",
+                    help="ffma: FP32 CUDA-core kernels (the headline); tf32x3: 3xTF32 "
+                         "tensor-core variant, reported separately")
     ap.add_argument("--alpha", type=float, default=1.0, help="C = alpha*A.B + beta*C")
     ap.add_argument("--beta", type=float, default=0.0)
     args = ap.parse_args(argv)
@@ -380,7 +489,7 @@ def main(argv=None):
     ctx = (rank, world, local)
     names = sorted(WORKLOADS, key=lambda n: WORKLOADS[n].flops) if args.sweep else [w.name]
     for name in names:
-        line = bench_gpu(args, WORKLOADS[name], ctx)
+        line = (bench_tf32x3 if args.path == "tf32x3" else bench_gpu)(args, WORKLOADS[name], ctx)
         if line is not None and rank == 0:
             if not args.no_cpu_baseline and world == 1 and not args.sweep:
                 A, B = make_inputs(WORKLOADS[name])

@@ -46,6 +46,14 @@ SIGNATURES = {
     "sgemm_query_config": (_i, [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                                 ctypes.POINTER(SgemmConfig)]),
     "sgemm_run_host": (_i, _RUN + [_vp, _vp, _vp, _vp]),
+    "sgemm_tf32x3_run": (_i, _RUN + [_vp]),
+    "sgemm_tf32x3_run_ex": (_i, [_i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, ctypes.c_float,
+                                 _vp, _i, _vp, _sz, _vp]),
+    "sgemm_tf32x3_workspace_size": (_i, [_i, _i, _i, ctypes.POINTER(_sz)]),
+    "sgemm_tf32x3_prepare": (_i, _RUN[:7] + [_vp, _sz, _vp]),
+    "sgemm_tf32x3_multiply": (_i, [_i, _i, _i, ctypes.c_float, ctypes.c_float, _vp, _i, _vp, _sz,
+                                   _vp]),
+    "sgemm_device_status": (_i, []),
     "sgemm_schedule_check": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(SgemmConfig)]),
     "sgemm_num_kernels": (_i, []),
     "sgemm_kernel_info": (_i, [_i, ctypes.POINTER(SgemmConfig)]),

@@ -621,6 +621,112 @@ int sgemm_schedule_check(int M, int N, int K, int kernel_id, int sms, int ctas_p
     return check_schedule(p, t_last_error, sizeof(t_last_error));
 }
 
+int sgemm_tf32x3_workspace_size(int M, int N, int K, size_t* out_bytes) {
+    if (out_bytes == nullptr || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    *out_bytes = tf32x3_workspace_bytes(M, N, K);
+    return SGEMM_OK;
+}
+
+int sgemm_tf32x3_run_ex(int M, int N, int K, float alpha, const float* A, int lda,
+                        const float* B, int ldb, float beta, float* C, int ldc, void* ws,
+                        size_t ws_bytes, sgemm_stream_t stream) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+    if (rc != SGEMM_OK) return rc;
+    if (!(alpha == alpha) || !(beta == beta)) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "alpha or beta is NaN");
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    if (M == 0 || N == 0) return SGEMM_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error("cudaGetDevice", e);
+        return SGEMM_ERR_UNSUPPORTED;
+    }
+    const DeviceInfo* d = nullptr;
+    rc = device_info(dev, &d);
+    if (rc != SGEMM_OK) return rc;
+    if (K == 0 || alpha == 0.0f) return launch_scale(C, M, N, ldc, beta, s, d);
+    const size_t need = tf32x3_workspace_bytes(M, N, K);
+    if (ws == nullptr) {
+        rc = library_workspace(s, need, &ws);
+        if (rc != SGEMM_OK) return rc;
+        ws_bytes = need;
+    } else if (ws_bytes < need || !aligned16(ws)) {
+        std::snprintf(t_last_error, sizeof(t_last_error),
+                      "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+        return SGEMM_ERR_WORKSPACE;
+    }
+    const int c_vec = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    rc = tf32x3_prepare(M, N, K, A, lda, B, ldb, ws, ws_bytes, d->sms, s);
+    g_launches.fetch_add(2, std::memory_order_relaxed);
+    if (rc != SGEMM_OK) return rc;
+    rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, ws, ws_bytes, d->sms, s);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return rc;
+}
+
+int sgemm_tf32x3_prepare(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                         void* ws, size_t ws_bytes, sgemm_stream_t stream) {
+    int rc = check_args(M, N, K, A, lda, B, ldb, reinterpret_cast<const float*>(ws), std::max(N, 1));
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0 || K == 0) return SGEMM_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_UNSUPPORTED;
+    const DeviceInfo* d = nullptr;
+    rc = device_info(dev, &d);
+    if (rc != SGEMM_OK) return rc;
+    if (!aligned16(ws)) return SGEMM_ERR_WORKSPACE;
+    rc = tf32x3_prepare(M, N, K, A, lda, B, ldb, ws, ws_bytes,
+                        d->sms, reinterpret_cast<cudaStream_t>(stream));
+    g_launches.fetch_add(2, std::memory_order_relaxed);
+    return rc;
+}
+
+int sgemm_tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, int ldc,
+                          const void* ws, size_t ws_bytes, sgemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0 || ldc < std::max(N, 1) || (M > 0 && N > 0 && C == nullptr) ||
+        !(alpha == alpha) || !(beta == beta)) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "invalid argument");
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    if (M == 0 || N == 0) return SGEMM_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_UNSUPPORTED;
+    const DeviceInfo* d = nullptr;
+    int rc = device_info(dev, &d);
+    if (rc != SGEMM_OK) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0 || alpha == 0.0f) return launch_scale(C, M, N, ldc, beta, s, d);
+    if (ws == nullptr || !aligned16(ws)) return SGEMM_ERR_WORKSPACE;
+    const int c_vec = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, const_cast<void*>(ws), ws_bytes,
+                         d->sms, s);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return rc;
+}
+
+int sgemm_tf32x3_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+                     float* C, int ldc, sgemm_stream_t stream) {
+    return sgemm_tf32x3_run_ex(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, nullptr, 0, stream);
+}
+
+int sgemm_device_status(void) {
+    int flag = 0;
+    const int rc = tf32x3_read_and_clear_timeout(&flag);
+    if (rc != SGEMM_OK) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "cannot read the device status word");
+        return rc;
+    }
+    if (flag) {
+        std::snprintf(t_last_error, sizeof(t_last_error),
+                      "a bounded wait in a tensor-core kernel gave up");
+        return SGEMM_ERR_TIMEOUT;
+    }
+    return SGEMM_OK;
+}
+
 int sgemm_num_kernels(void) { return static_cast<int>(table().size()); }
 
 int sgemm_kernel_info(int kernel_id, sgemm_config* out) {

@@ -50,4 +50,12 @@ int reduce_chunks(int bm, int bn, int sk_tiles, int sms);
 // Sets the text sgemm_last_error() returns on this thread.
 void set_last_error_message(const char* msg);
 
+// 3xTF32 tensor-core path (sgemm_tf32x3.cu).
+size_t tf32x3_workspace_bytes(int M, int N, int K);
+int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const float* B,
+                   long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
+int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
+                    int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
+int tf32x3_read_and_clear_timeout(int* flag);
+
 }  // namespace sgemm

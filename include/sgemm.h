@@ -165,6 +165,42 @@ SGEMM_API int sgemm_run_host(int M, int N, int K, const float* hA, int lda, cons
                    float* hC, int ldc, float* dA, float* dB, float* dC,
                    sgemm_stream_t stream);
 
+/* 3xTF32 tensor-core variant (tcgen05, TMEM, TMA): C = alpha * A.B + beta * C with
+ * each operand split into two TF32 numbers, x = hi + lo, and
+ * A.B ~= Ahi.Bhi + Ahi.Blo + Alo.Bhi accumulated in fp32 in tensor memory
+ * ("Register/Shared Memory Tiling", 관련 개념 / 장단점: pairing the tile
+ * hierarchy with tensor-core MMA).  Accuracy is FP32-class but not the CUDA-core
+ * path's: the tolerance is max|C - C_ref| <= 1e-5 * K * max|A| * max|B|.  Inf and
+ * NaN inputs are not supported (the split turns Inf into NaN).  The split
+ * operands go to a workspace of sgemm_tf32x3_workspace_size() bytes: the caller's
+ * `ws` (16-byte aligned, ws_bytes large enough) or, when ws is NULL, the library's
+ * per-stream workspace (allocated on first use).  Launches three kernels (two
+ * splits, one GEMM).  Any alignment of A, B, C and any leading dimensions.
+ * Bounded device-side waits that give up set a flag read by sgemm_device_status(). */
+SGEMM_API int sgemm_tf32x3_run(int M, int N, int K, const float* A, int lda, const float* B,
+                               int ldb, float* C, int ldc, sgemm_stream_t stream);
+SGEMM_API int sgemm_tf32x3_run_ex(int M, int N, int K, float alpha, const float* A, int lda,
+                                  const float* B, int ldb, float beta, float* C, int ldc,
+                                  void* ws, size_t ws_bytes, sgemm_stream_t stream);
+SGEMM_API int sgemm_tf32x3_workspace_size(int M, int N, int K, size_t* out_bytes);
+
+/* The two steps of sgemm_tf32x3_run_ex, for callers that reuse operands or time
+ * the steps apart.  _prepare writes the TF32 hi/lo parts of A (M x K) and the
+ * transposed parts of B (K x N) into `ws` (caller-owned, 16-byte aligned, at
+ * least sgemm_tf32x3_workspace_size(M, N, K) bytes); _multiply then computes
+ * C = alpha * A.B + beta * C from that workspace only.  Both are asynchronous
+ * on `stream`; the workspace must not change between them. */
+SGEMM_API int sgemm_tf32x3_prepare(int M, int N, int K, const float* A, int lda, const float* B,
+                                   int ldb, void* ws, size_t ws_bytes, sgemm_stream_t stream);
+SGEMM_API int sgemm_tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C,
+                                    int ldc, const void* ws, size_t ws_bytes,
+                                    sgemm_stream_t stream);
+
+/* Synchronous: reads and clears the device flag that a bounded wait in a
+ * tensor-core kernel sets when it gives up; returns SGEMM_ERR_TIMEOUT if it was
+ * set, SGEMM_OK otherwise.  Call after synchronising the work in question. */
+SGEMM_API int sgemm_device_status(void);
+
 /* Host-only check of the persistent / stream-K schedule (no GPU needed): plans
  * M x N x K for tile-table entry `kernel_id` as if `sms` SMs each held
  * `ctas_per_sm` CTAs, then walks every CTA's list of k-slices the way the kernel
