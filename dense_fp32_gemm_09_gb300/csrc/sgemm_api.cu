@@ -15,14 +15,17 @@
 #include <utility>
 #include <vector>
 
+#include "sgemm_ffma_tma.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_sched.cuh"
+#include "sgemm_tma_host.h"
 
 namespace sgemm {
 
 const KernelEntry* ffma_entries_main(int* count);
 const KernelEntry* ffma_entries_small(int* count);
 const KernelEntry* ffma_entries_any(int* count);
+const KernelEntry* ffma_entries_tma(int* count);
 
 namespace {
 
@@ -46,6 +49,8 @@ const std::vector<KernelEntry>& table() {
         e = ffma_entries_small(&n);
         v.insert(v.end(), e, e + n);
         e = ffma_entries_any(&n);
+        v.insert(v.end(), e, e + n);
+        e = ffma_entries_tma(&n);
         v.insert(v.end(), e, e + n);
         return v;
     }();
@@ -199,7 +204,7 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
     else if (tiles128 * 4 < d.sms)
         name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
     else if (v4)
-        name = K >= 2048 ? "128x256x64_t8x16_s2_f2_v4" : "128x256x32_t8x16_s4_f2_v4";
+        name = K >= 2048 ? "128x256x64_t8x16_s2_f2_v4" : "128x256x32_t8x16_s4_f2_tma";
     else
         name = "128x256x32_t8x16_s3_f2_v1";
     return find_entry(name);
@@ -337,7 +342,20 @@ int launch(const Plan& p, cudaStream_t stream) {
     cfg.numAttrs = 0;
     GemmArgs args = p.args;
     void* params[] = {&args};
-    cudaError_t err = cudaLaunchKernelExC(&cfg, e.kernel, params);
+    FfmaTmaParams tp;
+    void* tma_params[] = {&tp};
+    if (e.tma) {
+        // A: 32 (k) x BM boxes, 128-byte swizzle; B: BN (n) x BK boxes, no swizzle.
+        tp.g = p.args;
+        if (!encode_fp32_2d(&tp.ta, p.args.A, p.args.M, p.args.K, p.args.lda, 32, e.bm, true) ||
+            !encode_fp32_2d(&tp.tb, p.args.B, p.args.K, p.args.N, p.args.ldb, e.bn, e.bk,
+                            false)) {
+            std::snprintf(t_last_error, sizeof(t_last_error),
+                          "%s: cuTensorMapEncodeTiled failed", e.name);
+            return SGEMM_ERR_LAUNCH;
+        }
+    }
+    cudaError_t err = cudaLaunchKernelExC(&cfg, e.kernel, e.tma ? tma_params : params);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) {
@@ -382,6 +400,7 @@ int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const fl
     if (rc != SGEMM_OK) return rc;
     p.args.alpha = alpha;
     p.args.beta = beta;
+    p.args.status = status_word_ptr();
     p.args.epi = (beta != 0.0f) ? kEpiAlphaBeta : (alpha != 1.0f ? kEpiAlpha : kEpiPlain);
     const size_t need = p.ws_partial_bytes;
     if (need > 0) {
@@ -714,14 +733,14 @@ int sgemm_tf32x3_run(int M, int N, int K, const float* A, int lda, const float* 
 
 int sgemm_device_status(void) {
     int flag = 0;
-    const int rc = tf32x3_read_and_clear_timeout(&flag);
+    const int rc = read_and_clear_status(&flag);
     if (rc != SGEMM_OK) {
         std::snprintf(t_last_error, sizeof(t_last_error), "cannot read the device status word");
         return rc;
     }
     if (flag) {
         std::snprintf(t_last_error, sizeof(t_last_error),
-                      "a bounded wait in a tensor-core kernel gave up");
+                      "a bounded wait in a TMA-fed kernel gave up");
         return SGEMM_ERR_TIMEOUT;
     }
     return SGEMM_OK;

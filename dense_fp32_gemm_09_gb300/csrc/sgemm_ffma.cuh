@@ -409,7 +409,7 @@ constexpr KernelEntry make_entry(const char* name) {
     return KernelEntry{name,
                        reinterpret_cast<const void*>(&sgemm_ffma_kernel<Cfg>),
                        Cfg::BM, Cfg::BN, Cfg::BK, Cfg::WM, Cfg::WN, Cfg::TM, Cfg::TN,
-                       Cfg::STAGES, Cfg::NT, Cfg::SMEM_BYTES, Cfg::VEC, Cfg::FMA2 ? 1 : 0};
+                       Cfg::STAGES, Cfg::NT, Cfg::SMEM_BYTES, Cfg::VEC, Cfg::FMA2 ? 1 : 0, 0};
 }
 
 }  // namespace sgemm

@@ -31,16 +31,23 @@ struct GemmArgs {
     int group_m;           // tile rasterisation: tile rows per group
 
     float* ws_partial;     // [G][2][BM*BN] partial tiles of split tiles
+    int* status;           // device status word (bounded waits that give up)
 };
 
 // One entry of the tile table.
 struct KernelEntry {
     const char* name;
-    const void* kernel;     // __global__ void(GemmArgs)
+    const void* kernel;     // __global__ void(GemmArgs) or void(FfmaTmaParams) when tma
     int bm, bn, bk, wm, wn, tm, tn, stages, threads, smem_bytes;
     int vec;                // 4: needs 16-byte aligned A/B rows; 1: any alignment
     int fma2;
+    int tma;                // 1: operands staged by TMA (tensor maps built per call)
 };
+
+// Device status word (sgemm_status.cu): address on the current device, and a
+// synchronous read-and-clear of its value.
+int* status_word_ptr();
+int read_and_clear_status(int* value);
 
 // Sums the partial tiles of a stream-K launch into C (sgemm_reduce.cu).  Launch
 // it on the same stream right after the main kernel when a.sk_tiles > 0.
@@ -56,6 +63,6 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
                    long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
 int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
                     int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
-int tf32x3_read_and_clear_timeout(int* flag);
+
 
 }  // namespace sgemm

@@ -21,8 +21,9 @@
 //     finished accumulator to the epilogue;
 //   * warps 2..5: read the accumulator with tcgen05.ld (each warp its 32 TMEM
 //     lanes = 32 rows of the tile) and store C, then free the accumulator.
-// Every mbarrier wait is bounded in time; a wait that gives up records a flag
-// (read by sgemm_device_status) and the CTA drains and exits instead of hanging.
+// Every mbarrier wait is bounded in time; a wait that gives up writes the
+// library's device status word (read by sgemm_device_status) and the CTA drains
+// and exits instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -32,19 +33,23 @@
 #include <cstdio>
 #include <mutex>
 
+#include "sgemm_async.cuh"
 #include "sgemm_internal.h"
 
 namespace sgemm {
 namespace tc {
 
-__device__ int g_tc_timeout = 0;
+using async::gtimer;
+using async::mbar_arrive;
+using async::mbar_expect_tx;
+using async::mbar_init;
+using async::su32;
+using async::tma_load_2d;
 
 constexpr int BM = 128;
 constexpr int BK = 32;        // fp32 per k-block row: one 128-byte swizzle row
 constexpr int UMMA_K = 8;     // K of one tcgen05.mma .kind::tf32
 constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr unsigned long long kWaitNs = 4000000000ull;  // 4 s per wait
-constexpr unsigned kMaxSpins = 1u << 30;
 
 // Workspace regions are padded to 256 bytes (TMA wants 16-byte aligned bases).
 inline size_t align_up_floats(size_t n) { return (n + 63) / 64 * 64; }
@@ -58,64 +63,12 @@ struct Params {
     int c_vec;
     int epi;
     float alpha, beta;
+    int* status;      // device status word for waits that give up
 };
 
 // ----------------------------------------------------------------------------
 // PTX wrappers
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t su32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long gtimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Waits for the phase of `bar` with parity `parity`.  Gives up (returns false)
-// when another role has aborted or after kWaitNs / kMaxSpins, recording a timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = gtimer();
-    for (unsigned i = 1; i < kMaxSpins; ++i) {
-        if (mbar_try(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort) return false;
-            if (gtimer() - t0 > kWaitNs) break;
-        }
-    }
-    atomicExch(&g_tc_timeout, 1);
-    *abort = 1;
-    return false;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -265,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
                 int m0, n0;
                 tile_mn(p, tile, BN, m0, n0);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!mbar_wait(su32(&empty_bar[stage]), phase ^ 1u, abort_flag)) {
+                    if (!async::mbar_wait(su32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -288,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
                 // Aborting: let copies already in flight land before the CTA exits.
                 volatile int no_abort = 0;
                 for (int s = 0; s < STAGES; ++s)
-                    if (issued[s]) mbar_wait(su32(&full_bar[s]), issued_phase[s], &no_abort);
+                    if (issued[s]) async::mbar_wait(su32(&full_bar[s]), issued_phase[s], &no_abort, nullptr);
             }
         }
     } else if (warp == 1) {
@@ -302,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
                 for (int c = 0; ok && c < chunks; ++c) {
-                    if (!mbar_wait(su32(&tempty_bar[buf]), buf_phase ^ 1u, abort_flag)) {
+                    if (!async::mbar_wait(su32(&tempty_bar[buf]), buf_phase ^ 1u, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -310,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
                     const int kb_end = min(p.kblocks, (c + 1) * KC_BLOCKS);
                     for (int kb = c * KC_BLOCKS; kb < kb_end; ++kb) {
-                        if (!mbar_wait(su32(&full_bar[stage]), phase, abort_flag)) {
+                        if (!async::mbar_wait(su32(&full_bar[stage]), phase, abort_flag, p.status)) {
                             ok = false;
                             break;
                         }
@@ -355,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
 #pragma unroll
             for (int i = 0; i < BN; ++i) sum[i] = 0.0f;
             for (int c = 0; c < chunks; ++c) {
-                if (!mbar_wait(su32(&tfull_bar[buf]), buf_phase, abort_flag)) {
+                if (!async::mbar_wait(su32(&tfull_bar[buf]), buf_phase, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
@@ -594,6 +547,7 @@ int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long
     p.alpha = alpha;
     p.beta = beta;
     p.epi = (beta != 0.0f) ? kEpiAlphaBeta : (alpha != 1.0f ? kEpiAlpha : kEpiPlain);
+    p.status = status_word_ptr();
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = std::min(tiles, sms);
     tf32x3_kernel<kBN, kStages, kChunkBlocks><<<grid, kThreads, kSmemBytes, stream>>>(p);
@@ -601,19 +555,6 @@ int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long
         set_last_error_message("tf32x3: GEMM kernel failed to launch");
         return SGEMM_ERR_LAUNCH;
     }
-    return SGEMM_OK;
-}
-
-int tf32x3_read_and_clear_timeout(int* flag) {
-    int v = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, tc::g_tc_timeout, sizeof(int));
-    if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    if (v) {
-        const int zero = 0;
-        e = cudaMemcpyToSymbol(tc::g_tc_timeout, &zero, sizeof(int));
-        if (e != cudaSuccess) return SGEMM_ERR_LAUNCH;
-    }
-    *flag = v;
     return SGEMM_OK;
 }
 
