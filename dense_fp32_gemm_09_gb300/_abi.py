@@ -54,6 +54,7 @@ SIGNATURES = {
     "sgemm_tf32x3_multiply": (_i, [_i, _i, _i, ctypes.c_float, ctypes.c_float, _vp, _i, _vp, _sz,
                                    _vp]),
     "sgemm_device_status": (_i, []),
+    "sgemm_selftest_bounded_wait": (_i, [_i]),
     "sgemm_schedule_check": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(SgemmConfig)]),
     "sgemm_num_kernels": (_i, []),
     "sgemm_kernel_info": (_i, [_i, ctypes.POINTER(SgemmConfig)]),

@@ -746,6 +746,16 @@ int sgemm_device_status(void) {
     return SGEMM_OK;
 }
 
+int sgemm_selftest_bounded_wait(int limit_ms) {
+    if (limit_ms < 1 || limit_ms > 10000) return SGEMM_ERR_INVALID_ARG;
+    const int rc = run_wait_selftest(limit_ms);
+    if (rc != SGEMM_OK) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "self-test kernel failed to run");
+        return rc;
+    }
+    return sgemm_device_status();
+}
+
 int sgemm_num_kernels(void) { return static_cast<int>(table().size()); }
 
 int sgemm_kernel_info(int kernel_id, sgemm_config* out) {

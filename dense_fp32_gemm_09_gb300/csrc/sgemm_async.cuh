@@ -48,14 +48,15 @@ __device__ __forceinline__ unsigned long long gtimer() {
 // when *abort is set by another thread, or after kWaitNs / kMaxSpins; then it
 // records kStatusWaitTimeout in *status (if given) and sets *abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          int* status) {
+                                          int* status,
+                                          unsigned long long limit_ns = kWaitNs) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = gtimer();
     for (unsigned i = 1; i < kMaxSpins; ++i) {
         if (mbar_try(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort) return false;
-            if (gtimer() - t0 > kWaitNs) break;
+            if (gtimer() - t0 > limit_ns) break;
         }
     }
     if (status) atomicExch(status, kStatusWaitTimeout);

@@ -48,6 +48,7 @@ struct KernelEntry {
 // synchronous read-and-clear of its value.
 int* status_word_ptr();
 int read_and_clear_status(int* value);
+int run_wait_selftest(int limit_ms);
 
 // Sums the partial tiles of a stream-K launch into C (sgemm_reduce.cu).  Launch
 // it on the same stream right after the main kernel when a.sk_tiles > 0.
@@ -63,6 +64,7 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
                    long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
 int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
                     int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
+int tf32x3_tile_width(int M, int N, int sms);
 
 
 }  // namespace sgemm

@@ -9,6 +9,7 @@
 
 #include <mutex>
 
+#include "sgemm_async.cuh"
 #include "sgemm_internal.h"
 
 namespace sgemm {
@@ -44,6 +45,33 @@ int read_and_clear_status(int* value) {
             return SGEMM_ERR_LAUNCH;
     }
     *value = v;
+    return SGEMM_OK;
+}
+
+namespace {
+
+// One CTA waits on an mbarrier that nothing ever arrives on: the bounded wait
+// must give up by itself after limit_ns and record the timeout.
+__global__ void wait_selftest_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_s;
+    if (threadIdx.x == 0) {
+        async::mbar_init(async::su32(&bar), 1);
+        abort_s = 0;
+        async::mbar_fence_init();
+    }
+    __syncthreads();
+    async::mbar_wait(async::su32(&bar), 0, &abort_s, status, limit_ns);
+}
+
+}  // namespace
+
+int run_wait_selftest(int limit_ms) {
+    int* status = status_word_ptr();
+    if (status == nullptr) return SGEMM_ERR_LAUNCH;
+    wait_selftest_kernel<<<1, 32>>>(status, static_cast<unsigned long long>(limit_ms) * 1000000ull);
+    if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+        return SGEMM_ERR_LAUNCH;
     return SGEMM_OK;
 }
 

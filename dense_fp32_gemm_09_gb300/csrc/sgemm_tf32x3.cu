@@ -31,6 +31,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "sgemm_async.cuh"
@@ -49,7 +50,8 @@ using async::tma_load_2d;
 constexpr int BM = 128;
 constexpr int BK = 32;        // fp32 per k-block row: one 128-byte swizzle row
 constexpr int UMMA_K = 8;     // K of one tcgen05.mma .kind::tf32
-constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+// warp 0: TMA, warp 1: MMA, then 4 epilogue warps per 128 accumulator columns
+__host__ __device__ constexpr int tf32x3_threads(int bn) { return 64 + 32 * 4 * (bn / 128); }
 
 // Workspace regions are padded to 256 bytes (TMA wants 16-byte aligned bases).
 inline size_t align_up_floats(size_t n) { return (n + 63) / 64 * 64; }
@@ -157,12 +159,14 @@ __device__ __forceinline__ float epi_one(const Params& p, float acc, const float
 // registers with round-to-nearest adds.  Two TMEM chunk buffers alternate so the
 // MMAs of chunk c+1 overlap the epilogue's read of chunk c.
 template <int BN, int STAGES, int KC_BLOCKS>
-__global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(tf32x3_threads(BN), 1)
+    tf32x3_kernel(const __grid_constant__ Params p) {
+    constexpr int EPI_WARPS = 4 * (BN / 128);
     constexpr uint32_t A_BYTES = BM * BK * 4;
     constexpr uint32_t B_BYTES = BN * BK * 4;
     constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     constexpr uint32_t TMEM_COLS = 2 * BN;   // two chunk accumulators
-    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+    static_assert(BN == 128 || BN == 256, "BN");
     static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
                   "TMEM allocation must be a power of two");
 
@@ -187,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(su32(&tfull_bar[b]), 1);
-            mbar_init(su32(&tempty_bar[b]), 4);
+            mbar_init(su32(&tempty_bar[b]), EPI_WARPS);
         }
         abort_s = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -297,16 +301,21 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
         }
     } else {
         // ---------------- epilogue: TMEM chunks -> fp32 sums -> C ----------------
-        const int q = warp & 3;   // this warp may read TMEM lanes [32q, 32q + 32)
+        // Warp w may read TMEM lanes [32 (w % 4), +32) = 32 rows of the tile; the
+        // epilogue warps come in groups of four, group g owning columns
+        // [128 g, 128 g + 128).
+        constexpr int EC = 128;            // accumulator columns per epilogue warp
+        const int q = warp & 3;
+        const int col0 = EC * ((warp - 2) / 4);
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
             int m0, n0;
             tile_mn(p, tile, BN, m0, n0);
-            float sum[BN];
+            float sum[EC];
 #pragma unroll
-            for (int i = 0; i < BN; ++i) sum[i] = 0.0f;
+            for (int i = 0; i < EC; ++i) sum[i] = 0.0f;
             for (int c = 0; c < chunks; ++c) {
                 if (!async::mbar_wait(su32(&tfull_bar[buf]), buf_phase, abort_flag, p.status)) {
                     ok = false;
@@ -314,11 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
                 }
                 tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < BN / 32; ++j) {
+                for (int j = 0; j < EC / 32; ++j) {
                     float v[32];
                     __syncwarp();   // tcgen05.ld is warp-collective
                     tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
-                                  static_cast<uint32_t>(buf * BN + 32 * j),
+                                  static_cast<uint32_t>(buf * BN + col0 + 32 * j),
                               v);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) sum[32 * j + i] += v[i];
@@ -334,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1) tf32x3_kernel(const __grid_consta
             if (row < p.M) {
                 float* crow = p.C + static_cast<long long>(row) * p.ldc;
 #pragma unroll
-                for (int j = 0; j < BN / 32; ++j) {
-                    const int c0 = n0 + 32 * j;
+                for (int j = 0; j < EC / 32; ++j) {
+                    const int c0 = n0 + col0 + 32 * j;
                     if (p.c_vec && c0 + 31 < p.N) {
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
@@ -425,10 +434,16 @@ __global__ void split_bt_kernel(const float* __restrict__ B, long long ldb, int 
 // ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
-constexpr int kBN = 128;
-constexpr int kStages = 3;
 constexpr int kChunkBlocks = 4;   // 128 of K per TMEM chunk
-constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * (2 * BM * BK * 4 + 2 * kBN * BK * 4) + 1024;
+// Two output-tile widths: 128 columns with 3 pipeline stages, or 256 columns
+// with 2 (the shared-memory ring holds 192 KB either way).
+template <int BN>
+struct Variant {
+    static constexpr int kStages = BN == 256 ? 2 : 3;
+    static constexpr int kThreads = tf32x3_threads(BN);
+    static constexpr size_t kSmem =
+        static_cast<size_t>(kStages) * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024;
+};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -507,31 +522,35 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
     return SGEMM_OK;
 }
 
-int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
-                    int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream) {
+namespace {
+
+// Fraction of the last wave of `tiles` tiles over `ctas` CTAs that does work.
+double wave_efficiency(long long tiles, int ctas) {
+    const long long waves = (tiles + ctas - 1) / ctas;
+    return static_cast<double>(tiles) / static_cast<double>(waves * ctas);
+}
+
+template <int BN>
+int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
+                   int c_vec, const WsLayout& L, int Kp, int sms, cudaStream_t stream) {
     using namespace tc;
+    using V = Variant<BN>;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tf32x3_kernel<kBN, kStages, kChunkBlocks>,
+        attr_err = cudaFuncSetAttribute(tf32x3_kernel<BN, V::kStages, kChunkBlocks>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kSmemBytes));
+                                        static_cast<int>(V::kSmem));
     });
     if (attr_err != cudaSuccess) {
         set_last_error_message("tf32x3: cannot set the kernel's shared-memory size");
         return SGEMM_ERR_LAUNCH;
     }
-    if (ws == nullptr || ws_bytes < tf32x3_workspace_bytes(M, N, K)) {
-        set_last_error_message("tf32x3: workspace too small");
-        return SGEMM_ERR_WORKSPACE;
-    }
-    const int Kp = (K + 3) / 4 * 4;
-    const WsLayout L = ws_layout(ws, M, N, Kp);
     Params p{};
     if (!encode_kmajor(&p.tm_ahi, L.ahi, M, K, Kp, BM) ||
         !encode_kmajor(&p.tm_alo, L.alo, M, K, Kp, BM) ||
-        !encode_kmajor(&p.tm_bhi, L.bhi, N, K, Kp, kBN) ||
-        !encode_kmajor(&p.tm_blo, L.blo, N, K, Kp, kBN)) {
+        !encode_kmajor(&p.tm_bhi, L.bhi, N, K, Kp, BN) ||
+        !encode_kmajor(&p.tm_blo, L.blo, N, K, Kp, BN)) {
         set_last_error_message("tf32x3: cuTensorMapEncodeTiled failed");
         return SGEMM_ERR_LAUNCH;
     }
@@ -541,7 +560,7 @@ int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long
     p.N = N;
     p.K = K;
     p.tiles_m = (M + BM - 1) / BM;
-    p.tiles_n = (N + kBN - 1) / kBN;
+    p.tiles_n = (N + BN - 1) / BN;
     p.kblocks = (K + BK - 1) / BK;
     p.c_vec = c_vec;
     p.alpha = alpha;
@@ -550,12 +569,42 @@ int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long
     p.status = status_word_ptr();
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = std::min(tiles, sms);
-    tf32x3_kernel<kBN, kStages, kChunkBlocks><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    tf32x3_kernel<BN, V::kStages, kChunkBlocks><<<grid, V::kThreads, V::kSmem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) {
         set_last_error_message("tf32x3: GEMM kernel failed to launch");
         return SGEMM_ERR_LAUNCH;
     }
     return SGEMM_OK;
+}
+
+}  // namespace
+
+int tf32x3_tile_width(int M, int N, int sms) {
+    if (const char* force = std::getenv("SGEMM_TF32X3_BN")) {
+        const int bn = std::atoi(force);
+        if (bn == 128 || bn == 256) return bn;
+    }
+    // 256-wide tiles run about 5 % faster per tile (each MMA re-reads A for twice
+    // the columns) but quantise into fewer, larger waves and pad narrow C more:
+    // pick the better expected efficiency.
+    const long long tm = (M + tc::BM - 1) / tc::BM;
+    const long long t128 = (N + 127) / 128, t256 = (N + 255) / 256;
+    const double e128 = wave_efficiency(tm * t128, sms) * N / (128.0 * t128);
+    const double e256 = wave_efficiency(tm * t256, sms) * N / (256.0 * t256);
+    return e256 * 1.05 > e128 ? 256 : 128;
+}
+
+int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
+                    int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream) {
+    if (ws == nullptr || ws_bytes < tf32x3_workspace_bytes(M, N, K)) {
+        set_last_error_message("tf32x3: workspace too small");
+        return SGEMM_ERR_WORKSPACE;
+    }
+    const int Kp = (K + 3) / 4 * 4;
+    const WsLayout L = ws_layout(ws, M, N, Kp);
+    if (tf32x3_tile_width(M, N, sms) == 256)
+        return launch_variant<256>(M, N, K, alpha, beta, C, ldc, c_vec, L, Kp, sms, stream);
+    return launch_variant<128>(M, N, K, alpha, beta, C, ldc, c_vec, L, Kp, sms, stream);
 }
 
 }  // namespace sgemm

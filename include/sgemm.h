@@ -201,6 +201,14 @@ SGEMM_API int sgemm_tf32x3_multiply(int M, int N, int K, float alpha, float beta
  * set, SGEMM_OK otherwise.  Call after synchronising the work in question. */
 SGEMM_API int sgemm_device_status(void);
 
+/* Failure-detection self-test (synchronous): launches one CTA that waits, with
+ * the same time-bounded mbarrier wait the TMA-fed kernels use but a limit of
+ * `limit_ms` (1..10000), on a barrier that nothing completes.  The wait must
+ * give up by itself and record the timeout; returns SGEMM_ERR_TIMEOUT when it
+ * did (the expected result, read and cleared through sgemm_device_status), and
+ * SGEMM_OK if the wait was never recorded.  The context stays usable. */
+SGEMM_API int sgemm_selftest_bounded_wait(int limit_ms);
+
 /* Host-only check of the persistent / stream-K schedule (no GPU needed): plans
  * M x N x K for tile-table entry `kernel_id` as if `sms` SMs each held
  * `ctas_per_sm` CTAs, then walks every CTA's list of k-slices the way the kernel

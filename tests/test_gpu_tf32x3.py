@@ -31,10 +31,20 @@ def run(torch, A, B, C=None, alpha=1.0, beta=0.0, lda=None, ldb=None):
     return C
 
 
+@pytest.fixture(params=["auto", "128", "256"])
+def tile_width(request, monkeypatch):
+    """Run with the library's choice of tile width, then forced to each width."""
+    if request.param == "auto":
+        monkeypatch.delenv("SGEMM_TF32X3_BN", raising=False)
+    else:
+        monkeypatch.setenv("SGEMM_TF32X3_BN", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 256, 32), (1, 1, 1), (5, 7, 3), (128, 256, 64),
                                    (129, 257, 33), (300, 500, 1000), (1000, 333, 77),
                                    (2048, 64, 4096)])
-def test_shapes(cuda, oracle_mod, M, N, K):
+def test_shapes(cuda, oracle_mod, tile_width, M, N, K):
     torch = cuda
     A, B = random_pair(M, N, K, seed=M + 3 * N + 7 * K)
     C = run(torch, A.cuda(), B.cuda())
@@ -44,7 +54,7 @@ def test_shapes(cuda, oracle_mod, M, N, K):
 
 
 @pytest.mark.parametrize("name", ["sgemm_1024", "sgemm_2048", "sgemm_ragged_3001x2047x1999"])
-def test_workloads(cuda, oracle_mod, name):
+def test_workloads(cuda, oracle_mod, tile_width, name):
     torch = cuda
     A, B = make_inputs(name)
     C = run(torch, A.cuda(), B.cuda())
@@ -84,7 +94,7 @@ def test_split_matters(cuda, oracle_mod):
     assert np.max(np.abs(C.cpu().numpy() - ref)) <= 1e-6 * 512 * 4   # far below TF32 alone
 
 
-def test_strided_and_scaled(cuda, oracle_mod):
+def test_strided_and_scaled(cuda, oracle_mod, tile_width):
     torch = cuda
     A, B = random_pair(300, 200, 150, seed=9)
     dA = torch.full((300, 153), float("nan"), device="cuda")
