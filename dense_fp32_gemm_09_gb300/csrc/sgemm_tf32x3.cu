@@ -392,41 +392,76 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
     lo = __uint_as_float(r);
 }
 
-// Ahi/Alo[i*Kp + k] for i < M, k < Kp (zeros for K <= k < Kp).
-__global__ void split_a_kernel(const float* __restrict__ A, long long lda, int M, int K, int Kp,
-                               float* __restrict__ hi, float* __restrict__ lo) {
-    const long long total = static_cast<long long>(M) * Kp;
-    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
-         e += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long i = e / Kp;
-        const int k = static_cast<int>(e - i * Kp);
-        float h = 0.f, l = 0.f;
-        if (k < K) split_tf32(A[i * lda + k], h, l);
-        hi[e] = h;
-        lo[e] = l;
+// Ahi/Alo[i*Kp + k] for i < M, k < Kp (zeros for K <= k < Kp).  Each thread
+// writes 4 consecutive k of one row as one float4 of hi and one of lo; it reads
+// A with a float4 too when the row is 16-byte aligned (vec_in) and whole.
+__global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ A, long long lda,
+                                                      int M, int K, int Kp, int vec_in,
+                                                      float* __restrict__ hi,
+                                                      float* __restrict__ lo) {
+    const int k = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (k >= Kp) return;
+    for (int i = blockIdx.y; i < M; i += gridDim.y) {
+        const float* arow = A + static_cast<long long>(i) * lda;
+        float x[4];
+        if (vec_in && k + 3 < K) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(arow + k));
+            x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) x[u] = (k + u < K) ? __ldg(arow + k + u) : 0.0f;
+        }
+        float h[4], l[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) split_tf32(x[u], h[u], l[u]);
+        const long long o = static_cast<long long>(i) * Kp + k;
+        *reinterpret_cast<float4*>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<float4*>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
     }
 }
 
-// Bhi/Blo[n*Kp + k] = split(B[k*ldb + n]) for n < N, k < Kp, through a 32x32 tile.
-__global__ void split_bt_kernel(const float* __restrict__ B, long long ldb, int K, int N, int Kp,
-                                float* __restrict__ hi, float* __restrict__ lo) {
-    __shared__ float th[32][33];
-    __shared__ float tl[32][33];
-    const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
-    const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
-    for (int r = ty; r < 32; r += 8) {
-        const int k = k0 + r, n = n0 + tx;
-        float h = 0.f, l = 0.f;
-        if (k < K && n < N) split_tf32(B[static_cast<long long>(k) * ldb + n], h, l);
-        th[r][tx] = h;
-        tl[r][tx] = l;
+// Bhi/Blo[n*Kp + k] = split(B[k*ldb + n]) for n < N, k < Kp, through a 64 x 64
+// shared tile: reads along n and writes along k, both as float4 (reads fall back
+// to scalars when B's rows are not 16-byte aligned).
+constexpr int kTT = 64;
+__global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__ B, long long ldb,
+                                                       int K, int N, int Kp, int vec_in,
+                                                       float* __restrict__ hi,
+                                                       float* __restrict__ lo) {
+    __shared__ float th[kTT][kTT + 1];
+    __shared__ float tl[kTT][kTT + 1];
+    const int k0 = blockIdx.y * kTT, n0 = blockIdx.x * kTT;
+    const int c4 = (threadIdx.x & 15) * 4;   // 16 threads x 4 columns per row
+    const int r0 = threadIdx.x >> 4;         // 16 rows per pass
+#pragma unroll
+    for (int pass = 0; pass < kTT / 16; ++pass) {
+        const int r = r0 + 16 * pass;        // k within the tile
+        const int k = k0 + r, n = n0 + c4;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (k < K) {
+            const float* brow = B + static_cast<long long>(k) * ldb;
+            if (vec_in && n + 3 < N) {
+                const float4 t = __ldg(reinterpret_cast<const float4*>(brow + n));
+                x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) x[u] = (n + u < N) ? __ldg(brow + n + u) : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) split_tf32(x[u], th[r][c4 + u], tl[r][c4 + u]);
     }
     __syncthreads();
-    for (int r = ty; r < 32; r += 8) {
-        const int n = n0 + r, k = k0 + tx;
+#pragma unroll
+    for (int pass = 0; pass < kTT / 16; ++pass) {
+        const int nr = r0 + 16 * pass;       // n within the tile
+        const int n = n0 + nr, k = k0 + c4;
         if (n < N && k < Kp) {
-            hi[static_cast<long long>(n) * Kp + k] = th[tx][r];
-            lo[static_cast<long long>(n) * Kp + k] = tl[tx][r];
+            const long long o = static_cast<long long>(n) * Kp + k;
+            *reinterpret_cast<float4*>(hi + o) =
+                make_float4(th[c4][nr], th[c4 + 1][nr], th[c4 + 2][nr], th[c4 + 3][nr]);
+            *reinterpret_cast<float4*>(lo + o) =
+                make_float4(tl[c4][nr], tl[c4 + 1][nr], tl[c4 + 2][nr], tl[c4 + 3][nr]);
         }
     }
 }
@@ -509,12 +544,17 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
     }
     const int Kp = (K + 3) / 4 * 4;
     const WsLayout L = ws_layout(ws, M, N, Kp);
-    const long long total = static_cast<long long>(M) * Kp;
-    const long long blocks = std::min<long long>((total + 255) / 256, 8LL * sms);
-    split_a_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(A, lda, M, K, Kp, L.ahi,
-                                                                       L.alo);
-    dim3 grid((N + 31) / 32, (Kp + 31) / 32);
-    split_bt_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, ldb, K, N, Kp, L.bhi, L.blo);
+    (void)sms;
+    if ((Kp + kTT - 1) / kTT > 65535) {
+        set_last_error_message("tf32x3: K too large for the split kernels' grid");
+        return SGEMM_ERR_UNSUPPORTED;
+    }
+    const int a_vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0 && lda % 4 == 0) ? 1 : 0;
+    const int b_vec = ((reinterpret_cast<uintptr_t>(B) & 15) == 0 && ldb % 4 == 0) ? 1 : 0;
+    const dim3 ga((Kp / 4 + 255) / 256, std::min(M, 65535));
+    split_a_kernel<<<ga, 256, 0, stream>>>(A, lda, M, K, Kp, a_vec, L.ahi, L.alo);
+    const dim3 gb((N + kTT - 1) / kTT, (Kp + kTT - 1) / kTT);
+    split_bt_kernel<<<gb, 256, 0, stream>>>(B, ldb, K, N, Kp, b_vec, L.bhi, L.blo);
     if (cudaGetLastError() != cudaSuccess) {
         set_last_error_message("tf32x3: split kernels failed to launch");
         return SGEMM_ERR_LAUNCH;
