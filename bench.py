@@ -40,7 +40,9 @@ def describe(w) -> str:
     return f"{w.name}: M={w.M} N={w.N} K={w.K} fp32 row-major, A,B ~ {dist} seed {w.seed}"
 
 
-KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_internal.h", "sgemm_kernels_main.cu"]
+# Files whose text is the code of the FFMA kernels (the tile-table entry name
+# encodes the template parameters).
+KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_internal.h", "sgemm_epilogue.cuh"]
 
 
 def kernel_sources_hash() -> str:

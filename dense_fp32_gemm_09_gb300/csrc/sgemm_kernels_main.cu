@@ -9,6 +9,7 @@ namespace sgemm {
 // large-problem workhorses; BK = 64 halves the per-slice overhead when K is long.
 using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 4, true, 1>;
 using W256K32 = FfmaCfg<128, 256, 32, 8, 16, 4, 4, 2, 4, 4, 4, true, 1>;
+using W256K16 = FfmaCfg<128, 256, 16, 8, 16, 4, 4, 2, 6, 4, 4, true, 1>;
 using H256K64 = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1>;
 // Two CTAs per SM with 8 x 8 tiles (128 registers).
 using S128K32 = FfmaCfg<128, 128, 32, 8, 8, 4, 4, 2, 3, 4, 4, true, 2>;
@@ -18,6 +19,7 @@ using S128F1 = FfmaCfg<128, 128, 16, 8, 8, 4, 4, 2, 4, 4, 4, false, 2>;
 static const KernelEntry kEntries[] = {
     make_entry<W256K64>("128x256x64_t8x16_s2_f2_v4"),
     make_entry<W256K32>("128x256x32_t8x16_s4_f2_v4"),
+    make_entry<W256K16>("128x256x16_t8x16_s6_f2_v4"),
     make_entry<H256K64>("256x128x64_t8x16_s2_f2_v4"),
     make_entry<S128K32>("128x128x32_t8x8_s3_f2_v4"),
     make_entry<S128F1>("128x128x16_t8x8_s4_f1_v4"),

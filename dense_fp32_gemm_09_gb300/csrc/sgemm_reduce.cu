@@ -79,6 +79,11 @@ int reduce_chunks(int bm, int bn, int sk_tiles, int sms) {
 }
 
 cudaError_t launch_sk_reduce(const GemmArgs& a, int bm, int bn, int sms, cudaStream_t stream) {
+    // Same shared-memory carveout preference as the GEMM kernels, so the SMs need
+    // not be reconfigured between the two launches.
+    static const cudaError_t carveout = cudaFuncSetAttribute(
+        sk_reduce_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    (void)carveout;
     int chunks = reduce_chunks(bm, bn, a.sk_tiles, sms);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(a.sk_tiles) * chunks);

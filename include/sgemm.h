@@ -81,13 +81,18 @@ typedef struct {
     int sk_tiles;          /* tiles completed by more than one CTA (stream-K) */
     int ctas_per_sm;       /* resident CTAs per SM for this kernel */
     int fma2;              /* 1: packed fma.rn.f32x2 micro-kernel */
+    int packed;            /* sgemm_run copies A (bit 0) / B (bit 1) to aligned buffers first */
 } sgemm_config;
 
 /* C = A.B on `stream`.  One kernel launch, plus a second, short reduction launch
  * when the schedule splits the K range of some tiles between CTAs (stream-K);
  * the partial tiles then go to a library-owned device workspace (allocated on
  * first use per device and stream with the stream-ordered allocator, grown when
- * a larger one is needed, freed by sgemm_shutdown).  The first call that needs
+ * a larger one is needed, freed by sgemm_shutdown).  Large problems (M*N*K >=
+ * 2^31) whose A or B rows are not 16-byte aligned are first copied row by row
+ * into aligned buffers in that workspace (one more launch per copied operand),
+ * so they run on the 16-byte / TMA kernels; the results are the same as without
+ * the copy (the copy moves values, not sums).  The first call that needs
  * a workspace must not be made while the stream is being captured into a CUDA
  * graph. */
 SGEMM_API int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb,

@@ -294,7 +294,9 @@ def test_query_config_matches_bench_choice(cuda):
     assert cfg["grid"] > 0 and cfg["tiles"] == (4096 // cfg["bm"]) * (4096 // cfg["bn"])
     assert cfg["ctas_per_sm"] >= 1
     rag = sgemm_query_config(3001, 2047, 1999)
-    assert rag["vec"] == 1   # odd leading dimensions: 4-byte loads
+    assert rag["packed"] == 3 and rag["vec"] == 4   # odd ld: copied to aligned buffers
+    small = sgemm_query_config(301, 205, 199)
+    assert small["packed"] == 0 and small["vec"] == 1   # too small to be worth copying
 
 
 def test_launch_counter_counts(cuda):
@@ -304,3 +306,22 @@ def test_launch_counter_counts(cuda):
     n0 = launch_count()
     sgemm(A, A)
     assert launch_count() == n0 + 1
+
+
+def test_large_unaligned_operands_are_packed(cuda, oracle_mod):
+    """M*N*K >= 2^31 with rows off 16-byte alignment: sgemm_run copies the operands
+    to aligned buffers first (reported by sgemm_query_config) and the result
+    still matches the oracle, with nothing written outside C."""
+    torch = cuda
+    M, N, K = 1100, 1500, 1401
+    A, B = random_pair(M, N, K, seed=77)
+    dA = padded(torch, A, 2, offset=1)      # lda = 1403, base 4-byte aligned only
+    dB = padded(torch, B, 1, offset=2)      # ldb = 1501
+    cfg = sgemm_query_config(M, N, K, 1403, 1501, N + 3, dA.data_ptr(), dB.data_ptr(), None)
+    assert cfg["packed"] == 3 and cfg["vec"] == 4
+    buf, C = canaried(torch, M, N, ldc_pad=3)
+    sgemm(dA, dB, out=C)
+    torch.cuda.synchronize()
+    check_canary(buf, M, N)
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+    assert np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref)) <= tolerance(A, B)
