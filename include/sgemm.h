@@ -163,9 +163,17 @@ SGEMM_API int sgemm_query_config(int M, int N, int K, int lda, int ldb, int ldc,
 
 /* Host-buffer convenience for end-to-end use: copies A and B from host memory
  * (pinned for full speed) into the caller's device buffers dA, dB (row-major,
- * leading dimensions lda, ldb), runs sgemm_run into dC (leading dimension ldc),
- * and copies C back to hC, all on `stream`.  The call returns when the work is
- * queued; synchronise the stream before reading hC. */
+ * leading dimensions lda, ldb), computes C = A.B into dC (leading dimension ldc)
+ * and copies C back to hC.  The work is ordered after everything already queued
+ * on `stream`, and `stream` waits for all of it, so it behaves as if issued on
+ * `stream`; inside, it runs on three library-owned streams of the current device
+ * (created on first use, destroyed by sgemm_shutdown): B is copied first, then A
+ * and C go in row panels of C, so that one panel's copies overlap another
+ * panel's product.  The call returns when the work is queued; synchronise
+ * `stream` before reading hC.  Calls from several host threads are serialised
+ * while they queue.  Errors: as sgemm_run, plus SGEMM_ERR_INVALID_ARG for a null
+ * device buffer with a non-empty extent and SGEMM_ERR_LAUNCH for a failed copy;
+ * after an error, `stream` is still ordered after whatever part was queued. */
 SGEMM_API int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* hB, int ldb,
                    float* hC, int ldc, float* dA, float* dB, float* dC,
                    sgemm_stream_t stream);

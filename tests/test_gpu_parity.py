@@ -289,6 +289,64 @@ def test_host_buffer_entry_point(cuda, oracle_mod):
     assert np.max(np.abs(hC.numpy() - ref)) <= tolerance(A, B)
 
 
+@pytest.mark.parametrize("panels", ["1", "3", "7"])
+@pytest.mark.parametrize("M,N,K", [(1000, 333, 257), (130, 64, 40), (515, 96, 0)])
+def test_host_entry_row_panels(cuda, oracle_mod, monkeypatch, panels, M, N, K):
+    """The host-buffer entry in 1, 3 and 7 row panels (ragged last panel, padded
+    leading dimensions, K == 0) on a side stream matches the oracle."""
+    torch = cuda
+    from dense_fp32_gemm_09_gb300 import check, sgemm_run_host
+    monkeypatch.setenv("SGEMM_HOST_PANELS", panels)
+    A, B = random_pair(M, N, K, seed=11)
+    lda, ldb, ldc = K + 3, N + 1, N + 2
+    hA = torch.zeros(M, lda).pin_memory()
+    hB = torch.zeros(K, ldb).pin_memory()
+    hA[:, :K] = A
+    hB[:, :N] = B
+    hC = torch.full((M, ldc), SENTINEL).pin_memory()
+    dA = torch.empty(M * lda + 1, device="cuda")
+    dB = torch.empty(K * ldb + 1, device="cuda")
+    dC = torch.full((M * ldc + 1,), SENTINEL, device="cuda")
+    side = torch.cuda.Stream()
+    check(sgemm_run_host(M, N, K, hA.data_ptr(), lda, hB.data_ptr(), ldb, hC.data_ptr(), ldc,
+                         dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream=side),
+          "sgemm_run_host")
+    side.synchronize()
+    got = hC.numpy()
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy()) if K > 0 else np.zeros((M, N))
+    assert np.max(np.abs(got[:, :N] - ref)) <= (tolerance(A, B) if K > 0 else 0.0)
+    assert np.all(got[:, N:] == SENTINEL)
+
+
+def test_host_entry_is_ordered_on_the_callers_stream(cuda, oracle_mod, monkeypatch):
+    """Work queued on the stream before the call finishes before the call's
+    copies and products start, and work queued after it sees the finished C."""
+    torch = cuda
+    from dense_fp32_gemm_09_gb300 import check, sgemm_run_host
+    monkeypatch.setenv("SGEMM_HOST_PANELS", "4")
+    M, N, K = 1024, 512, 384
+    A, B = random_pair(M, N, K, seed=12)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.empty(M, N).pin_memory()
+    dA = torch.empty(M, K, device="cuda")
+    dB = torch.empty(K, N, device="cuda")
+    dC = torch.empty(M, N, device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(50_000_000)        # tens of milliseconds of GPU time
+        dC.fill_(float("nan"))               # must land before the product
+        check(sgemm_run_host(M, N, K, hA.data_ptr(), K, hB.data_ptr(), N, hC.data_ptr(), N,
+                             dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), stream=side),
+              "sgemm_run_host")
+        after = dC.clone()                   # must see the finished product
+    side.synchronize()
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+    tol = tolerance(A, B)
+    assert np.max(np.abs(hC.numpy() - ref)) <= tol
+    assert np.max(np.abs(after.cpu().numpy() - ref)) <= tol
+    assert torch.equal(after, dC)
+
+
 def test_query_config_matches_bench_choice(cuda):
     cfg = sgemm_query_config(4096, 4096, 4096)
     assert cfg["grid"] > 0 and cfg["tiles"] == (4096 // cfg["bm"]) * (4096 // cfg["bn"])
