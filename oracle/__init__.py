@@ -59,7 +59,10 @@ def _load():
         d = ctypes.c_double
         lib.oracle_gemm_f64_ex.argtypes = [i, i, i, d, f32p, i64, f32p, i64, d, f32p, i64,
                                            i32p, i, f64p, i]
+        lib.oracle_gemm_f64_op.argtypes = [i, i, i, i, i, d, f32p, i64, f32p, i64, d, f32p,
+                                           i64, f64p, i]
         for fn in (lib.oracle_gemm_f64, lib.oracle_gemm_f64_rows, lib.oracle_gemm_f64_ex,
+                   lib.oracle_gemm_f64_op,
                    lib.oracle_gemm_f64_elems, lib.oracle_gemm_f32_fma_seq,
                    lib.oracle_max_threads):
             fn.restype = ctypes.c_int
@@ -180,6 +183,37 @@ def gemm_f64_ex(alpha, A, B, beta, C0, rows=None, nthreads: int | None = None) -
                                     _ptr(out, ctypes.c_double), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle_gemm_f64_ex rejected its arguments")
+    return out
+
+
+def gemm_f64_op(transa, transb, A, B, alpha=1.0, beta=0.0, C0=None,
+                nthreads: int | None = None) -> np.ndarray:
+    """alpha * op(A).op(B) + beta * C0 in double, op(X) = X^T where the flag is 1.
+
+    A and B are passed as STORED (row-major, possibly strided): with transa == 1,
+    A is K x M; with transb == 1, B is N x K."""
+    A, lda = _mat(A, "A")
+    B, ldb = _mat(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if transa else A.shape
+    KB, N = (B.shape[1], B.shape[0]) if transb else B.shape
+    if K != KB:
+        raise ValueError(f"inner dimensions differ: {K} vs {KB}")
+    if C0 is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C0")
+        C0 = np.zeros((1, max(N, 1)), dtype=np.float32)
+        ldc0 = max(N, 1)
+    else:
+        C0, ldc0 = _mat(C0, "C0")
+        if C0.shape != (M, N):
+            raise ValueError("C0 must be M x N")
+    out = np.empty((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_f64_op(int(transa), int(transb), M, N, K, float(alpha),
+                                    _ptr(A, ctypes.c_float), lda, _ptr(B, ctypes.c_float), ldb,
+                                    float(beta), _ptr(C0, ctypes.c_float), ldc0,
+                                    _ptr(out, ctypes.c_double), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_gemm_f64_op rejected its arguments")
     return out
 
 

@@ -166,6 +166,49 @@ int oracle_gemm_f64_ex(int M, int N, int K, double alpha, const float* A, int64_
     return 0;
 }
 
+/* Transposed operands, BLAS style, in double:
+ *   out[i][j] = alpha * sum_k opA[i][k] * opB[k][j] + beta * C0[i][j]
+ * with opA[i][k] = A[i*lda + k] (transa == 0, A stored M x K) or A[k*lda + i]
+ * (transa == 1, A stored K x M), and opB[k][j] = B[k*ldb + j] (transb == 0, B
+ * stored K x N) or B[j*ldb + k] (transb == 1, B stored N x K).  The product of
+ * the pages ("Register/Shared Memory Tiling", 관련 개념) taken on op(A), op(B);
+ * the same i -> k -> j loops and k order as above, only the reads change.
+ * beta == 0 does not read C0; alpha == 0 does not read A or B.  out is M x N
+ * with leading dimension N. */
+int oracle_gemm_f64_op(int transa, int transb, int M, int N, int K, double alpha,
+                       const float* A, int64_t lda, const float* B, int64_t ldb, double beta,
+                       const float* C0, int64_t ldc0, double* out, int nthreads)
+{
+    if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1)) return -1;
+    if (M < 0 || N < 0 || K < 0) return -1;
+    const int wa = transa ? M : K, wb = transb ? K : N;   /* stored row widths */
+    if (lda < (wa > 0 ? wa : 1) || ldb < (wb > 0 ? wb : 1) || ldc0 < (N > 0 ? N : 1)) return -1;
+    if (M > 0 && N > 0 && out == NULL) return -1;
+    if (alpha != 0.0 && K > 0 && M > 0 && N > 0 && (A == NULL || B == NULL)) return -1;
+    if (beta != 0.0 && M > 0 && N > 0 && C0 == NULL) return -1;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int i = 0; i < M; ++i) {
+        double* o = out + (int64_t)i * N;
+        for (int j = 0; j < N; ++j) o[j] = 0.0;
+        if (alpha != 0.0) {
+            for (int k = 0; k < K; ++k) {
+                const double a = transa ? (double)A[(int64_t)k * lda + i]
+                                        : (double)A[(int64_t)i * lda + k];
+                for (int j = 0; j < N; ++j) {
+                    const double b = transb ? (double)B[(int64_t)j * ldb + k]
+                                            : (double)B[(int64_t)k * ldb + j];
+                    o[j] += a * b;
+                }
+            }
+            for (int j = 0; j < N; ++j) o[j] *= alpha;
+        }
+        if (beta != 0.0)
+            for (int j = 0; j < N; ++j) o[j] += beta * (double)C0[(int64_t)i * ldc0 + j];
+    }
+    return 0;
+}
+
 /* Threads an OpenMP region would use here (for reporting the CPU baseline). */
 int oracle_max_threads(void)
 {

@@ -317,3 +317,108 @@ def test_ex_against_exact_rationals(oracle_mod, seed):
             want = Fraction(alpha) * exact[i][j] + Fraction(beta) * Fraction(float(C0[i, j]))
             bound = (K + 3) * u * (abs(alpha) * float(absum[i][j]) + abs(beta * float(C0[i, j])))
             assert abs(got[i, j] - float(want)) <= 1.01 * bound + 1e-300
+
+
+# --------------------------------------------------------------------------
+# transposed operands: op(A) . op(B)
+# --------------------------------------------------------------------------
+
+
+def stored(X, trans, pad=0):
+    """X (the logical operand) as the oracle receives it: X itself or its
+    transpose, optionally inside a NaN-padded row-major buffer (ld = width + pad)."""
+    S = np.ascontiguousarray(X.T if trans else X)
+    if pad == 0:
+        return S
+    buf = np.full((S.shape[0], S.shape[1] + pad), np.nan, dtype=np.float32)
+    buf[:, :S.shape[1]] = S
+    return buf[:, :S.shape[1]]
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("seed", range(3))
+def test_op_against_exact_rationals(oracle_mod, ta, tb, seed):
+    """The logical product is formed by hand in exact arithmetic from the
+    logical operands; the oracle gets them stored transposed where asked."""
+    rng = np.random.default_rng(400 + seed)
+    M, N, K = (int(x) for x in rng.integers(1, 8, size=3))
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    C0 = rng.standard_normal((M, N)).astype(np.float32)
+    alpha, beta = float(np.float32(1.5)), float(np.float32(0.25))
+    got = oracle_mod.gemm_f64_op(ta, tb, stored(A, ta, 3), stored(B, tb, 2), alpha, beta, C0)
+    exact, absum = exact_product(A, B)
+    u = 2.0 ** -53
+    for i in range(M):
+        for j in range(N):
+            want = Fraction(alpha) * exact[i][j] + Fraction(beta) * Fraction(float(C0[i, j]))
+            bound = (K + 3) * u * (abs(alpha) * float(absum[i][j]) + abs(beta * float(C0[i, j])))
+            assert abs(got[i, j] - float(want)) <= 1.01 * bound + 1e-300
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 1), (1, 0), (1, 1)])
+def test_op_small_integers_exact(oracle_mod, ta, tb):
+    rng = np.random.default_rng(7)
+    M, N, K = 37, 29, 53
+    A = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    B = rng.integers(-8, 9, (K, N)).astype(np.float32)
+    want = (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64)
+    got = oracle_mod.gemm_f64_op(ta, tb, stored(A, ta, 5), stored(B, tb, 1))
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 1), (1, 0), (1, 1)])
+def test_op_identity_and_permutation(oracle_mod, ta, tb):
+    rng = np.random.default_rng(8)
+    n = 23
+    X = rng.standard_normal((n, n)).astype(np.float32)
+    perm = rng.permutation(n)
+    P = np.zeros((n, n), dtype=np.float32)
+    P[np.arange(n), perm] = 1
+    I = np.eye(n, dtype=np.float32)
+    assert np.array_equal(oracle_mod.gemm_f64_op(ta, tb, stored(X, ta), stored(I, tb)),
+                          X.astype(np.float64))
+    assert np.array_equal(oracle_mod.gemm_f64_op(ta, tb, stored(P, ta), stored(X, tb)),
+                          X[perm].astype(np.float64))
+
+
+def test_op_rectangular_shapes_keep_their_roles(oracle_mod):
+    """M, N and K all differ, so a swapped role would change the output shape
+    or read the wrong extent."""
+    rng = np.random.default_rng(9)
+    M, N, K = 5, 3, 11
+    A = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    B = rng.integers(-4, 5, (K, N)).astype(np.float32)
+    want = (A.astype(np.int64) @ B.astype(np.int64)).astype(np.float64)
+    for ta in (0, 1):
+        for tb in (0, 1):
+            got = oracle_mod.gemm_f64_op(ta, tb, stored(A, ta), stored(B, tb))
+            assert got.shape == (M, N) and np.array_equal(got, want)
+
+
+def test_op_blas_conventions(oracle_mod):
+    rng = np.random.default_rng(10)
+    A = rng.standard_normal((6, 4)).astype(np.float32)    # stored K x M for transa
+    B = rng.standard_normal((5, 6)).astype(np.float32)    # stored N x K for transb
+    nan_c = np.full((4, 5), np.nan, dtype=np.float32)
+    assert np.all(np.isfinite(oracle_mod.gemm_f64_op(1, 1, A, B, 1.0, 0.0, nan_c)))
+    C0 = np.arange(20, dtype=np.float32).reshape(4, 5)
+    nan_a = np.full_like(A, np.nan)
+    nan_b = np.full_like(B, np.nan)
+    assert np.array_equal(oracle_mod.gemm_f64_op(1, 1, nan_a, nan_b, 0.0, 2.0, C0),
+                          2.0 * C0.astype(np.float64))
+
+
+def test_op_invalid_arguments_rejected(oracle_mod):
+    import ctypes
+    lib = oracle_mod._load()
+    f32p, f64p = ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double)
+    A = np.zeros((8, 8), dtype=np.float32)
+    out = np.zeros(64, dtype=np.float64)
+    pa = A.ctypes.data_as(f32p)
+    po = out.ctypes.data_as(f64p)
+    # transa == 1 with M = 8 needs lda >= 8; transb == 1 with K = 8 needs ldb >= 8
+    assert lib.oracle_gemm_f64_op(1, 0, 8, 4, 4, 1.0, pa, 4, pa, 8, 0.0, None, 4, po, 1) == -1
+    assert lib.oracle_gemm_f64_op(0, 1, 4, 4, 8, 1.0, pa, 8, pa, 4, 0.0, None, 4, po, 1) == -1
+    assert lib.oracle_gemm_f64_op(2, 0, 4, 4, 4, 1.0, pa, 8, pa, 8, 0.0, None, 4, po, 1) == -1
+    assert lib.oracle_gemm_f64_op(1, 1, 4, 4, 4, 1.0, pa, 8, pa, 8, 0.0, None, 4, po, 1) == 0

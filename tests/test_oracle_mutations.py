@@ -29,6 +29,10 @@ MUTATIONS = {
                      "one_row_f64(N, K, A + (int64_t)i * K,")],
     "drops_beta_term": [("o[j] += beta * (double)C0[(int64_t)i * ldc0 + j];",
                          "o[j] += 0.0 * (double)C0[(int64_t)i * ldc0 + j];")],
+    "op_ignores_transb": [("const double b = transb ? (double)B[(int64_t)j * ldb + k]",
+                           "const double b = transb ? (double)B[(int64_t)k * ldb + j]")],
+    "op_ignores_transa": [("const double a = transa ? (double)A[(int64_t)k * lda + i]",
+                           "const double a = transa ? (double)A[(int64_t)i * lda + k]")],
     "unfused_fp32": [("acc = fmaf(A[(int64_t)i * lda + k], B[(int64_t)k * ldb + j], acc);",
                       "acc = A[(int64_t)i * lda + k] * B[(int64_t)k * ldb + j] + acc;")],
 }
@@ -51,6 +55,8 @@ def build_variant(tmp_path, name):
     lib.oracle_gemm_f32_fma_seq.argtypes = [i, i, i, f32p, i64, f32p, i64, f32p, i64]
     lib.oracle_gemm_f64_ex.argtypes = [i, i, i, ctypes.c_double, f32p, i64, f32p, i64,
                                        ctypes.c_double, f32p, i64, ctypes.c_void_p, i, f64p, i]
+    lib.oracle_gemm_f64_op.argtypes = [i, i, i, i, i, ctypes.c_double, f32p, i64, f32p, i64,
+                                       ctypes.c_double, f32p, i64, f64p, i]
     return lib
 
 
@@ -97,6 +103,14 @@ def failing_pins(lib):
                            out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), 1)
     if not np.array_equal(out, 2 * want - 3 * C0.astype(np.float64)):
         fails.append("scaled_small_integers")
+    # transposed operands on small integers: op(A).op(B) with both stored transposed
+    out = np.empty((n, n), dtype=np.float64)
+    At, Bt = np.ascontiguousarray(A.T), np.ascontiguousarray(B.T)
+    lib.oracle_gemm_f64_op(1, 1, n, n, n, 1.0, At.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                           n, Bt.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), n, 0.0, None,
+                           n, out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), 1)
+    if not np.array_equal(out, want):
+        fails.append("op_small_integers")
     # the pages' printed worked example (fp32 mode)
     rows = {r[0]: r[1:] for r in read_golden("p1_micro_gemm_4x4.txt")}
     K = int(rows["K"][0])
