@@ -251,7 +251,27 @@ def bench_gpu(args, w, dist_ctx):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     scaled = args.alpha != 1.0 or args.beta != 0.0
-    if scaled:
+    ta, tb = args.trans[0] == "T", args.trans[1] == "T"
+    kid = getattr(args, "kernel_id", None)
+    if kid is not None:
+        # one forced tile-table entry (--tile-sweep); entries that cannot serve
+        # these operands are skipped
+        run_fn = lib.sgemm_run_with
+        run_args = (w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N, dC.data_ptr(), w.N,
+                    kid, 0, sh)
+        if run_fn(*run_args) == sg.SGEMM_ERR_UNSUPPORTED:
+            return None
+    elif ta or tb:
+        # the same logical operands, stored transposed where asked
+        sA = A.t().contiguous().to(dev) if ta else dA
+        sB = B.t().contiguous().to(dev) if tb else dB
+        if scaled:
+            dC.normal_()
+        run_fn = lib.sgemm_run_op
+        run_args = (int(ta), int(tb), w.M, w.N, w.K, args.alpha, sA.data_ptr(),
+                    w.M if ta else w.K, sB.data_ptr(), w.K if tb else w.N, args.beta,
+                    dC.data_ptr(), w.N, sh)
+    elif scaled:
         dC.normal_()
         run_fn = lib.sgemm_run_ex
         run_args = (w.M, w.N, w.K, args.alpha, dA.data_ptr(), w.K, dB.data_ptr(), w.N, args.beta,
@@ -260,8 +280,15 @@ def bench_gpu(args, w, dist_ctx):
         run_fn = lib.sgemm_run
         run_args = (w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N, dC.data_ptr(), w.N,
                     sh)
-    cfg = sg.sgemm_query_config(w.M, w.N, w.K, w.K, w.N, w.N, dA.data_ptr(), dB.data_ptr(),
-                                dC.data_ptr())
+    if kid is not None:
+        cfg = {k: None for k in ("grid", "tiles", "sk_tiles", "ctas_per_sm")}
+        cfg["name"] = sg.kernel_table()[kid]["name"]
+    elif ta or tb:   # the product runs on 16-byte-aligned transposed copies
+        cfg = sg.sgemm_query_config(w.M, w.N, w.K, (w.K + 3) // 4 * 4, (w.N + 3) // 4 * 4, w.N,
+                                    None, None, dC.data_ptr())
+    else:
+        cfg = sg.sgemm_query_config(w.M, w.N, w.K, w.K, w.N, w.N, dA.data_ptr(), dB.data_ptr(),
+                                    dC.data_ptr())
 
     def barrier():
         if world > 1:
@@ -293,7 +320,19 @@ def bench_gpu(args, w, dist_ctx):
     mean_ms = statistics.fmean(step_ms)
     med_ms, mean_ms = max_over_ranks([med_ms, mean_ms], dev)
 
-    # end to end through the host-buffer entry point: pinned host in, pinned host out
+    e2e_ms = None
+    if kid is None and not (ta or tb):   # the host entry takes row-major operands
+        e2e_ms = time_e2e(lib, check, A, B, w, dA, dB, dC, sh, stream, args, barrier, dev)
+
+    if rank != 0:
+        return None
+    return bench_line(args, w, world, med_ms, mean_ms, t_wall, e2e_ms, clocks, cfg, launches,
+                      scaled, dev)
+
+
+def time_e2e(lib, check, A, B, w, dA, dB, dC, sh, stream, args, barrier, dev):
+    """ms per step of the host-buffer entry point: pinned host in, pinned host out."""
+    import torch
     hA, hB = A.pin_memory(), B.pin_memory()
     hC = torch.empty(w.M, w.N).pin_memory()
     e2e_args = (w.M, w.N, w.K, hA.data_ptr(), w.K, hB.data_ptr(), w.N, hC.data_ptr(), w.N,
@@ -310,9 +349,12 @@ def bench_gpu(args, w, dist_ctx):
     barrier()
     e2e_ms = es.elapsed_time(ee) / e2e_steps
     (e2e_ms,) = max_over_ranks([e2e_ms], dev)
+    return e2e_ms
 
-    if rank != 0:
-        return None
+
+def bench_line(args, w, world, med_ms, mean_ms, t_wall, e2e_ms, clocks, cfg, launches, scaled,
+               dev):
+    import torch
     peaks = measured_peaks()
     props = torch.cuda.get_device_properties(dev)
     sms = props.multi_processor_count
@@ -322,6 +364,7 @@ def bench_gpu(args, w, dist_ctx):
     value = whole_job_tflops(world, flops, med_ms)
     achieved = flops / (med_ms * 1e-3) / 1e12
     clk = clocks.summary()
+    trans = args.trans != "NN"
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": med_ms,
@@ -329,7 +372,9 @@ def bench_gpu(args, w, dist_ctx):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": describe(w) + (f"; C = {args.alpha:g}*A.B + {args.beta:g}*C"
-                                              if scaled else ""),
+                                              if scaled else "")
+                   + (f"; operands {args.trans} (T = stored transposed, transposed on the "
+                      f"device inside the step)" if trans else ""),
                    "M": w.M, "N": w.N, "K": w.K,
                    "l2": "flushed before every step (256 MiB write, outside the events)",
                    "kernel": cfg["name"], "grid": cfg["grid"], "tiles": cfg["tiles"],
@@ -337,7 +382,7 @@ def bench_gpu(args, w, dist_ctx):
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops,
                      "unit": "TFLOP/s", "frac": achieved / peak_tflops,
-                     "traffic": recorded_traffic(cfg["name"], w.name),
+                     "traffic": None if trans else recorded_traffic(cfg["name"], w.name),
                      "algorithmic_bytes": w.min_bytes,
                      "peak_basis": f"{sms} SMs x {FMA_PER_CLK_PER_SM} FP32 FMA/clk x 2 x "
                                    f"{max_mhz:.0f} MHz (max SM clock)",
@@ -345,10 +390,11 @@ def bench_gpu(args, w, dist_ctx):
                          achieved / (sms * FMA_PER_CLK_PER_SM * 2 * clk["sm_mhz"] * 1e-6)
                          if clk.get("sm_mhz") else None)},
         "clocks": clk,
-        "e2e": {"value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
-                "d2h_bytes_per_step": 4 * w.M * w.N},
+        "e2e": None if e2e_ms is None else {
+            "value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
+            "ms_per_step": e2e_ms,
+            "h2d_bytes_per_step": 4 * (w.M * w.K + w.K * w.N),
+            "d2h_bytes_per_step": 4 * w.M * w.N},
         "gpu_launches": int(launches),
     }
     return line
@@ -474,6 +520,11 @@ def main(argv=None):
                          "tensor-core variant, reported separately")
     ap.add_argument("--alpha", type=float, default=1.0, help="C = alpha*A.B + beta*C")
     ap.add_argument("--beta", type=float, default=0.0)
+    ap.add_argument("--trans", choices=["NN", "NT", "TN", "TT"], default="NN",
+                    help="operands stored transposed (T) and multiplied as op(A).op(B)")
+    ap.add_argument("--tile-sweep", action="store_true",
+                    help="one line per tile-table entry that can serve the workload "
+                         "(forced entry, no e2e or CPU baseline)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -490,6 +541,14 @@ def main(argv=None):
         tdist.init_process_group("nccl")
     ctx = (rank, world, local)
     names = sorted(WORKLOADS, key=lambda n: WORKLOADS[n].flops) if args.sweep else [w.name]
+    if args.tile_sweep:
+        import dense_fp32_gemm_09_gb300 as sg
+        for kid in range(len(sg.kernel_table())):
+            args.kernel_id = kid
+            line = bench_gpu(args, w, ctx)
+            if line is not None and rank == 0:
+                print(json.dumps(line), flush=True)
+        names = []
     for name in names:
         line = (bench_tf32x3 if args.path == "tf32x3" else bench_gpu)(args, WORKLOADS[name], ctx)
         if line is not None and rank == 0:

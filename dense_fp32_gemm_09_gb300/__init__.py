@@ -12,7 +12,7 @@ from ._abi import (SGEMM_ERR_INVALID_ARG, SGEMM_ERR_LAUNCH, SGEMM_ERR_UNSUPPORTE
                    SGEMM_ERR_WORKSPACE, SGEMM_OK, SgemmConfig, SgemmError, check, load)
 
 __all__ = ["sgemm", "sgemm_run", "sgemm_run_ws", "sgemm_run_with", "sgemm_run_host",
-           "sgemm_run_noalloc", "sgemm_run_ex",
+           "sgemm_run_noalloc", "sgemm_run_ex", "sgemm_run_op",
            "sgemm_query_config", "sgemm_workspace_size", "kernel_table", "launch_count",
            "SgemmError", "load"]
 
@@ -31,6 +31,19 @@ def _ld(t, name: str) -> int:
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must have unit stride along its columns")
     return max(t.stride(0), t.shape[1], 1)
+
+
+def _layout(t, name: str) -> tuple[int, int]:
+    """(trans, ld) of a 2-D operand view: trans 0 for a row-major view (unit
+    column stride), 1 for the transpose of one (unit row stride, e.g. ``X.t()``)."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    rows, cols = t.shape
+    if cols <= 1 or t.stride(1) == 1:
+        return 0, max(t.stride(0), cols, 1)
+    if rows <= 1 or t.stride(0) == 1:
+        return 1, max(t.stride(1), rows, 1)
+    raise ValueError(f"{name} needs a unit stride along its rows or its columns")
 
 
 def _check_operand(t, name: str):
@@ -113,10 +126,19 @@ def sgemm_run_ex(M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, kerne
                                kernel_id, schedule, _stream_handle(stream))
 
 
+def sgemm_run_op(transa, transb, M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
+                 stream=None) -> int:
+    """Raw call of ``sgemm_run_op``: C = alpha * op(A).op(B) + beta * C, op = transpose
+    where the flag is 1 (A then stored K x M, B stored N x K)."""
+    return load().sgemm_run_op(transa, transb, M, N, K, alpha, A_ptr, lda, B_ptr, ldb, beta,
+                               C_ptr, ldc, _stream_handle(stream))
+
+
 def sgemm(A, B, out=None, *, alpha: float = 1.0, beta: float = 0.0,
           kernel_id: int | None = None, schedule: int = 0, stream=None):
-    """C = alpha * A @ B + beta * C for float32 CUDA tensors (row-major views with
-    unit column stride).
+    """C = alpha * A @ B + beta * C for float32 CUDA tensors.  A and B may be
+    row-major views (unit column stride) or transposes of them (``X.t()``, unit
+    row stride); ``out`` is a row-major view.
 
     ``out`` may be a preallocated (M, N) float32 CUDA view; with beta == 0 it is
     only written, otherwise its contents are the C of the formula (beta != 0
@@ -138,10 +160,16 @@ def sgemm(A, B, out=None, *, alpha: float = 1.0, beta: float = 0.0,
             raise ValueError(f"out must be {(M, N)}, got {tuple(out.shape)}")
     if M == 0 or N == 0:
         return out
-    lda, ldb, ldc = _ld(A, "A"), _ld(B, "B"), _ld(out, "out")
+    (ta, lda), (tb, ldb), ldc = _layout(A, "A"), _layout(B, "B"), _ld(out, "out")
     args = (M, N, K, A.data_ptr(), lda, B.data_ptr(), ldb, out.data_ptr(), ldc)
     with torch.cuda.device(A.device):
-        if alpha != 1.0 or beta != 0.0:
+        if ta or tb:
+            if kernel_id is not None or schedule != 0:
+                raise ValueError("kernel_id / schedule cannot be forced with transposed operands")
+            st = sgemm_run_op(ta, tb, M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(),
+                              ldb, float(beta), out.data_ptr(), ldc, stream=stream)
+            check(st, "sgemm_run_op")
+        elif alpha != 1.0 or beta != 0.0:
             st = sgemm_run_ex(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
                               float(beta), out.data_ptr(), ldc,
                               -1 if kernel_id is None else kernel_id, schedule, stream=stream)

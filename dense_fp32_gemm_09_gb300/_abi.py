@@ -40,6 +40,8 @@ SIGNATURES = {
     "sgemm_run_ws": (_i, _RUN + [_vp, _sz, _vp]),
     "sgemm_run_ex": (_i, [_i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, ctypes.c_float, _vp, _i,
                           _i, _i, _vp]),
+    "sgemm_run_op": (_i, [_i, _i, _i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, ctypes.c_float,
+                          _vp, _i, _vp]),
     "sgemm_run_noalloc": (_i, _RUN + [_vp]),
     "sgemm_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                                   ctypes.POINTER(_sz)]),

@@ -136,17 +136,22 @@ long long span(int rows, int cols, int ld) {
     return static_cast<long long>(rows - 1) * ld + cols;
 }
 
-int check_args(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-               const float* C, int ldc) {
+// Argument checks for C[M x N] = op(A)[M x K] . op(B)[K x N]: op(A) = A stored
+// M x K (transa == 0) or A^T with A stored K x M (transa == 1); likewise B.
+int check_args_op(int transa, int transb, int M, int N, int K, const float* A, int lda,
+                  const float* B, int ldb, const float* C, int ldc) {
     if (M < 0 || N < 0 || K < 0) {
         std::snprintf(t_last_error, sizeof(t_last_error), "negative size M=%d N=%d K=%d", M,
                       N, K);
         return SGEMM_ERR_INVALID_ARG;
     }
-    if (lda < std::max(K, 1) || ldb < std::max(N, 1) || ldc < std::max(N, 1)) {
+    const int ra = transa ? K : M, ca = transa ? M : K;   // stored A: ra x ca
+    const int rb = transb ? N : K, cb = transb ? K : N;   // stored B: rb x cb
+    if (lda < std::max(ca, 1) || ldb < std::max(cb, 1) || ldc < std::max(N, 1)) {
         std::snprintf(t_last_error, sizeof(t_last_error),
-                      "leading dimension below row width: lda=%d (K=%d) ldb=%d ldc=%d (N=%d)",
-                      lda, K, ldb, ldc, N);
+                      "leading dimension below row width: lda=%d (needs %d) ldb=%d (needs %d) "
+                      "ldc=%d (N=%d)",
+                      lda, ca, ldb, cb, ldc, N);
         return SGEMM_ERR_INVALID_ARG;
     }
     if ((M > 0 && N > 0 && C == nullptr) || (M > 0 && N > 0 && K > 0 && (A == nullptr ||
@@ -156,13 +161,18 @@ int check_args(int M, int N, int K, const float* A, int lda, const float* B, int
     }
     if (M > 0 && N > 0 && K > 0) {
         const long long sc = span(M, N, ldc);
-        if (ranges_overlap(C, sc, A, span(M, K, lda)) ||
-            ranges_overlap(C, sc, B, span(K, N, ldb))) {
+        if (ranges_overlap(C, sc, A, span(ra, ca, lda)) ||
+            ranges_overlap(C, sc, B, span(rb, cb, ldb))) {
             std::snprintf(t_last_error, sizeof(t_last_error), "C overlaps A or B");
             return SGEMM_ERR_INVALID_ARG;
         }
     }
     return SGEMM_OK;
+}
+
+int check_args(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
+               const float* C, int ldc) {
+    return check_args_op(0, 0, M, N, K, A, lda, B, ldb, C, ldc);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -500,13 +510,80 @@ int launch_pack(const float* src, long long lds, int rows, int cols, float* dst,
     return SGEMM_OK;
 }
 
+// Y = X^T: X is rows x cols (leading dimension ldx), Y is cols x rows (leading
+// dimension ldy, a multiple of 4, with Y 16-byte aligned; its padding columns are
+// not written).  64 x 64 tiles through shared memory (row stride 65), 256
+// threads: each moves four 16-byte chunks in and four out per tile, so a CTA has
+// 16 KB of loads in flight.  X is read as float4 when its rows are 16-byte
+// aligned, else element by element.  HBM-bound.
+__global__ void __launch_bounds__(256) transpose_kernel(const float* __restrict__ X,
+                                                        long long ldx, int rows, int cols,
+                                                        float* __restrict__ Y, long long ldy,
+                                                        int x_vec) {
+    constexpr int T = 64;
+    __shared__ float t[T][T + 1];
+    const long long tiles_c = (cols + T - 1) / T;
+    const long long tiles = tiles_c * ((rows + T - 1) / T);
+    for (long long tt = blockIdx.x; tt < tiles; tt += gridDim.x) {
+        const int r0 = static_cast<int>(tt / tiles_c) * T;
+        const int c0 = static_cast<int>(tt % tiles_c) * T;
+#pragma unroll
+        for (int e = threadIdx.x; e < T * T / 4; e += 256) {
+            const int r = e / (T / 4), c4 = (e % (T / 4)) * 4;
+            const int gr = r0 + r, gc = c0 + c4;
+            if (gr >= rows) continue;
+            const float* src = X + gr * ldx + gc;
+            if (x_vec && gc + 3 < cols) {
+                const float4 v = *reinterpret_cast<const float4*>(src);
+                t[r][c4] = v.x; t[r][c4 + 1] = v.y; t[r][c4 + 2] = v.z; t[r][c4 + 3] = v.w;
+            } else {
+                for (int q = 0; q < 4 && gc + q < cols; ++q) t[r][c4 + q] = src[q];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = threadIdx.x; e < T * T / 4; e += 256) {
+            const int c = e / (T / 4), r4 = (e % (T / 4)) * 4;
+            const int gy = c0 + c, gx = r0 + r4;   // Y[gy][gx..gx+3] = X[gx..gx+3][gy]
+            if (gy >= cols) continue;
+            float* dst = Y + gy * ldy + gx;
+            if (gx + 3 < rows) {
+                *reinterpret_cast<float4*>(dst) =
+                    make_float4(t[r4][c], t[r4 + 1][c], t[r4 + 2][c], t[r4 + 3][c]);
+            } else {
+                for (int q = 0; q < 4 && gx + q < rows; ++q) dst[q] = t[r4 + q][c];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+int launch_transpose(const float* X, long long ldx, int rows, int cols, float* Y, long long ldy,
+                     int sms, cudaStream_t stream) {
+    const long long tiles = ((rows + 63) / 64) * static_cast<long long>((cols + 63) / 64);
+    const int grid = static_cast<int>(std::max(1LL, std::min<long long>(tiles, 8LL * sms)));
+    const int x_vec = aligned16(X) && ldx % 4 == 0;
+    transpose_kernel<<<grid, 256, 0, stream>>>(X, ldx, rows, cols, Y, ldy, x_vec);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("transpose_kernel launch", e);
+        return SGEMM_ERR_LAUNCH;
+    }
+    return SGEMM_OK;
+}
+
 // Large problems whose A or B rows are not 16-byte aligned are worth copying to
 // aligned buffers first: the 4-byte-load kernels run ~16 % slower than the
 // 16-byte / TMA ones, the copy costs 8 bytes of traffic per operand element.
 constexpr double kPackMinMacs = 2147483648.0;   // M * N * K
 
+// Operand staging in the library workspace: a transposed operand is always
+// transposed into a row-major buffer; a misaligned one of a large problem is
+// copied row by row.  Staged buffers have 16-byte-aligned rows.
 struct PackPlan {
     bool pack_a = false, pack_b = false;
+    bool trans_a = false, trans_b = false;
     int lda = 0, ldb = 0;         // leading dimensions the kernels will see
     size_t bytes_a = 0, bytes_b = 0;
     const float* plan_a = nullptr;
@@ -514,17 +591,21 @@ struct PackPlan {
 };
 
 PackPlan pack_plan(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
-                   bool library_ws, int forced_entry) {
+                   bool library_ws, int forced_entry, int transa, int transb) {
     PackPlan q;
-    const bool pack = library_ws && forced_entry < 0 && !vec4_ok(A, lda, B, ldb) &&
+    q.trans_a = transa != 0;
+    q.trans_b = transb != 0;
+    // Each non-transposed operand is packed on its own: a transposed partner is
+    // staged aligned anyway, so the other one alone decides the load width.
+    const bool pack = library_ws && forced_entry < 0 &&
                       static_cast<double>(M) * N * K >= kPackMinMacs;
-    q.pack_a = pack && !(aligned16(A) && lda % 4 == 0);
-    q.pack_b = pack && !(aligned16(B) && ldb % 4 == 0);
+    q.pack_a = q.trans_a || (pack && !(aligned16(A) && lda % 4 == 0));
+    q.pack_b = q.trans_b || (pack && !(aligned16(B) && ldb % 4 == 0));
     q.lda = q.pack_a ? (K + 3) / 4 * 4 : lda;
     q.ldb = q.pack_b ? (N + 3) / 4 * 4 : ldb;
     q.bytes_a = q.pack_a ? align_up(static_cast<size_t>(M) * q.lda * 4, kWsAlign) : 0;
     q.bytes_b = q.pack_b ? align_up(static_cast<size_t>(K) * q.ldb * 4, kWsAlign) : 0;
-    // Alignment-only stand-ins for the packed buffers while planning.
+    // Alignment-only stand-ins for the staged buffers while planning.
     q.plan_a = q.pack_a ? reinterpret_cast<const float*>(uintptr_t{256}) : A;
     q.plan_b = q.pack_b ? reinterpret_cast<const float*>(uintptr_t{256} << 20) : B;
     return q;
@@ -533,8 +614,9 @@ PackPlan pack_plan(int M, int N, int K, const float* A, int lda, const float* B,
 // C = alpha * A.B + beta * C; the plain entry points pass alpha = 1, beta = 0.
 int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
              float beta, float* C, int ldc, int forced_entry, int schedule, void* ws,
-             size_t ws_bytes, bool library_ws, cudaStream_t stream) {
-    int rc = check_args(M, N, K, A, lda, B, ldb, C, ldc);
+             size_t ws_bytes, bool library_ws, cudaStream_t stream, int transa = 0,
+             int transb = 0) {
+    int rc = check_args_op(transa, transb, M, N, K, A, lda, B, ldb, C, ldc);
     if (rc != SGEMM_OK) return rc;
     if (M == 0 || N == 0) return SGEMM_OK;
     Plan p;
@@ -551,9 +633,16 @@ int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const fl
         if (rc != SGEMM_OK) return rc;
         return launch_scale(C, M, N, ldc, beta, stream, d);
     }
-    // Packing (library workspace only): misaligned operands are copied to
-    // aligned buffers at the front of the workspace and the plan is made for them.
-    const PackPlan q = pack_plan(M, N, K, A, lda, B, ldb, library_ws, forced_entry);
+    // Staging (library workspace only): transposed operands, and misaligned ones
+    // of large problems, are copied to aligned row-major buffers at the front of
+    // the workspace and the plan is made for them.
+    if ((transa || transb) && !library_ws) {
+        std::snprintf(t_last_error, sizeof(t_last_error),
+                      "transposed operands need the library workspace");
+        return SGEMM_ERR_UNSUPPORTED;
+    }
+    const PackPlan q = pack_plan(M, N, K, A, lda, B, ldb, library_ws, forced_entry, transa,
+                                 transb);
     const bool pack = q.pack_a || q.pack_b;
     const bool pack_a = q.pack_a, pack_b = q.pack_b;
     const int lda_p = q.lda, ldb_p = q.ldb;
@@ -573,13 +662,15 @@ int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const fl
         char* w = static_cast<char*>(base);
         if (pack_a) {
             float* pa = reinterpret_cast<float*>(w);
-            rc = launch_pack(A, lda, M, K, pa, lda_p, stream);
+            rc = q.trans_a ? launch_transpose(A, lda, K, M, pa, lda_p, d->sms, stream)
+                           : launch_pack(A, lda, M, K, pa, lda_p, stream);
             if (rc != SGEMM_OK) return rc;
             p.args.A = pa;
         }
         if (pack_b) {
             float* pb = reinterpret_cast<float*>(w + bytes_a);
-            rc = launch_pack(B, ldb, K, N, pb, ldb_p, stream);
+            rc = q.trans_b ? launch_transpose(B, ldb, N, K, pb, ldb_p, d->sms, stream)
+                           : launch_pack(B, ldb, K, N, pb, ldb_p, stream);
             if (rc != SGEMM_OK) return rc;
             p.args.B = pb;
         }
@@ -724,6 +815,22 @@ int sgemm_run_ex(int M, int N, int K, float alpha, const float* A, int lda, cons
                     0, true, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int sgemm_run_op(int transa, int transb, int M, int N, int K, float alpha, const float* A,
+                 int lda, const float* B, int ldb, float beta, float* C, int ldc,
+                 sgemm_stream_t stream) {
+    if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1)) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "transa=%d transb=%d (0 or 1)", transa,
+                      transb);
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    if (!(alpha == alpha) || !(beta == beta)) {
+        std::snprintf(t_last_error, sizeof(t_last_error), "alpha or beta is NaN");
+        return SGEMM_ERR_INVALID_ARG;
+    }
+    return run_impl(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, -1, 0, nullptr, 0, true,
+                    reinterpret_cast<cudaStream_t>(stream), transa, transb);
+}
+
 int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                  float* C, int ldc, void* ws, size_t ws_bytes, sgemm_stream_t stream) {
     return run_impl(M, N, K, 1.0f, A, lda, B, ldb, 0.0f, C, ldc, -1, 0, ws, ws_bytes, false,
@@ -773,7 +880,7 @@ int sgemm_query_config(int M, int N, int K, int lda, int ldb, int ldc, const flo
         return SGEMM_ERR_INVALID_ARG;
     Plan p;
     const DeviceInfo* d = nullptr;
-    const PackPlan q = pack_plan(M, N, K, pa, lda, pb, ldb, true, -1);
+    const PackPlan q = pack_plan(M, N, K, pa, lda, pb, ldb, true, -1, 0, 0);
     const int rc =
         plan(M, N, K, q.plan_a, q.lda, q.plan_b, q.ldb, const_cast<float*>(pc), ldc, -1, 0, p, &d);
     if (rc != SGEMM_OK) return rc;

@@ -161,6 +161,24 @@ SGEMM_API int sgemm_run_with(int M, int N, int K, const float* A, int lda, const
 SGEMM_API int sgemm_query_config(int M, int N, int K, int lda, int ldb, int ldc,
                        const float* A, const float* B, const float* C, sgemm_config* out);
 
+/* Transposed operands, BLAS style:  C = alpha * op(A) . op(B) + beta * C  with
+ * op(A) M x K and op(B) K x N.  transa == 0: A is stored M x K row-major
+ * (lda >= K); transa == 1: A is stored K x M row-major (lda >= M) and
+ * op(A) = A^T.  transb == 0: B is stored K x N (ldb >= N); transb == 1: B is
+ * stored N x K (ldb >= K) and op(B) = B^T.  C is M x N row-major (ldc >= N).
+ * Row-major with a transposed operand is the pages' product on op(A), op(B)
+ * ("Register/Shared Memory Tiling", 관련 개념: the tile hierarchy does not depend
+ * on which operand is stored k-major).  A transposed operand is first
+ * transposed into a 16-byte-aligned row-major buffer of the library workspace
+ * (an HBM-bound pass of 8 bytes per element), then the product runs on that
+ * buffer exactly as sgemm_run_ex would.  Device pointers, asynchronous on
+ * `stream`.  Errors: as sgemm_run_ex,
+ * plus SGEMM_ERR_INVALID_ARG for transa or transb other than 0 or 1, ld values
+ * below the stored row widths, or C overlapping the stored A or B. */
+SGEMM_API int sgemm_run_op(int transa, int transb, int M, int N, int K, float alpha,
+                           const float* A, int lda, const float* B, int ldb, float beta, float* C,
+                           int ldc, sgemm_stream_t stream);
+
 /* Host-buffer convenience for end-to-end use: copies A and B from host memory
  * (pinned for full speed) into the caller's device buffers dA, dB (row-major,
  * leading dimensions lda, ldb), computes C = A.B into dC (leading dimension ldc)
