@@ -70,7 +70,15 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-// Packed pair of fp32 accumulators: low 32 bits = column j, high = column j+1.
+// d += x * y elementwise on packed pairs (low 32 bits = column j, high = column
+// j+1); one multiplicand is two adjacent B values, the other one A value in both
+// halves.  The product is commutative; the operand order is a scheduling choice.
+__device__ __forceinline__ void ffma2(unsigned long long& d, unsigned long long x,
+                                      unsigned long long y) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(x), "l"(y));
+}
+
+// d += {a, a} * b: the A value broadcast into both halves inside the same asm.
 __device__ __forceinline__ void ffma2_bcast(unsigned long long& d, float a,
                                             unsigned long long b) {
     asm("{\n\t.reg .b64 ta;\n\t"
@@ -96,11 +104,13 @@ __device__ __forceinline__ float hi_f(unsigned long long x) {
 // ----------------------------------------------------------------------------
 // Register accumulators: plain fp32, or packed pairs for fma.rn.f32x2
 // ----------------------------------------------------------------------------
-template <int TM, int TN, bool FMA2>
+// BOUTER (packed form only): true = one B pair against every A value in turn,
+// false = one A value against every B pair.
+template <int TM, int TN, bool FMA2, bool BOUTER = true>
 struct Acc;
 
-template <int TM, int TN>
-struct Acc<TM, TN, false> {
+template <int TM, int TN, bool BOUTER>
+struct Acc<TM, TN, false, BOUTER> {
     float v[TM][TN];
     __device__ __forceinline__ void zero() {
 #pragma unroll
@@ -125,8 +135,8 @@ struct Acc<TM, TN, false> {
     }
 };
 
-template <int TM, int TN>
-struct Acc<TM, TN, true> {
+template <int TM, int TN, bool BOUTER>
+struct Acc<TM, TN, true, BOUTER> {
     unsigned long long v[TM][TN / 2];
     __device__ __forceinline__ void zero() {
 #pragma unroll
@@ -134,6 +144,10 @@ struct Acc<TM, TN, true> {
 #pragma unroll
             for (int j = 0; j < TN / 2; ++j) v[i][j] = 0ull;
     }
+    // B outer with B as the first multiplicand measured 1-3 % faster on the 8x16
+    // tile of the cp.async kernels; it keeps all TM broadcast pairs live, which
+    // the TMA kernel (A fragments for two k at once) cannot afford, so that one
+    // takes A outer.
     __device__ __forceinline__ void rank1(const float (&a)[TM], const float4 (&b)[TN / 4]) {
         unsigned long long bp[TN / 2];
 #pragma unroll
@@ -141,10 +155,20 @@ struct Acc<TM, TN, true> {
             bp[2 * j4] = pack2(b[j4].x, b[j4].y);
             bp[2 * j4 + 1] = pack2(b[j4].z, b[j4].w);
         }
+        if constexpr (BOUTER) {
+            unsigned long long ap[TM];
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < TM; ++i) ap[i] = pack2(a[i], a[i]);
 #pragma unroll
-            for (int j = 0; j < TN / 2; ++j) ffma2_bcast(v[i][j], a[i], bp[j]);
+            for (int j = 0; j < TN / 2; ++j)
+#pragma unroll
+                for (int i = 0; i < TM; ++i) ffma2(v[i][j], bp[j], ap[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN / 2; ++j) ffma2_bcast(v[i][j], a[i], bp[j]);
+        }
     }
     __device__ __forceinline__ float4 chunk(int i, int j4) const {
         return make_float4(lo_f(v[i][2 * j4]), hi_f(v[i][2 * j4]), lo_f(v[i][2 * j4 + 1]),

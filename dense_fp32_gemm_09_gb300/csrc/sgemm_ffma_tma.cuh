@@ -101,7 +101,7 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB)
     sgemm_ffma_tma_kernel(const __grid_constant__ FfmaTmaParams P) {
     using L = TmaLayout<Cfg>;
-    using AccT = Acc<Cfg::TM, Cfg::TN, Cfg::FMA2>;
+    using AccT = Acc<Cfg::TM, Cfg::TN, Cfg::FMA2, false>;
     constexpr int STAGES = Cfg::STAGES, BK = Cfg::BK;
     const GemmArgs& a = P.g;
 
