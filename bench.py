@@ -454,6 +454,8 @@ def bench_tf32x3(args, w, dist_ctx):
         barrier()
     launches = lib.sgemm_launch_count() - n0
     check(lib.sgemm_device_status(), "device status")
+    tcfg = sg.SgemmConfig()
+    check(lib.sgemm_tf32x3_query_config(w.M, w.N, w.K, ct.byref(tcfg)), "tf32x3 query")
     step_ms = statistics.median(e[0].elapsed_time(e[2]) for e in ev)
     split_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     gemm_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
@@ -490,7 +492,9 @@ def bench_tf32x3(args, w, dist_ctx):
         "data": "synthetic",
         "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
                    "l2": "flushed before every step (256 MiB write, outside the events)",
-                   "kernel": "tf32x3_kernel<BN=256, 2 stages> + split kernels",
+                   "kernel": f"tf32x3_kernel<BN={tcfg.bn}, {tcfg.stages} stages> + split "
+                             f"kernels" + (" + sk_reduce_kernel" if tcfg.sk_tiles else ""),
+                   "grid": tcfg.grid, "tiles": tcfg.tiles, "sk_tiles": tcfg.sk_tiles,
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "tensor", "achieved": 3 * flops / (gemm_ms * 1e-3) / 1e12,
                      "peak": peak, "unit": "TFLOP/s",

@@ -49,6 +49,7 @@ SIGNATURES = {
     "sgemm_query_config": (_i, [_i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                                 ctypes.POINTER(SgemmConfig)]),
     "sgemm_run_host": (_i, _RUN + [_vp, _vp, _vp, _vp]),
+    "sgemm_tf32x3_query_config": (_i, [_i, _i, _i, ctypes.POINTER(SgemmConfig)]),
     "sgemm_tf32x3_run": (_i, _RUN + [_vp]),
     "sgemm_tf32x3_run_ex": (_i, [_i, _i, _i, ctypes.c_float, _vp, _i, _vp, _i, ctypes.c_float,
                                  _vp, _i, _vp, _sz, _vp]),

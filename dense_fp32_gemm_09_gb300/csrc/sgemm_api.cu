@@ -1043,8 +1043,9 @@ int sgemm_tf32x3_run_ex(int M, int N, int K, float alpha, const float* A, int ld
     rc = tf32x3_prepare(M, N, K, A, lda, B, ldb, ws, ws_bytes, d->sms, s);
     g_launches.fetch_add(2, std::memory_order_relaxed);
     if (rc != SGEMM_OK) return rc;
-    rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, ws, ws_bytes, d->sms, s);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+    int n = 0;
+    rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, ws, ws_bytes, d->sms, s, &n);
+    g_launches.fetch_add(n, std::memory_order_relaxed);
     return rc;
 }
 
@@ -1082,10 +1083,22 @@ int sgemm_tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C
     if (K == 0 || alpha == 0.0f) return launch_scale(C, M, N, ldc, beta, s, d);
     if (ws == nullptr || !aligned16(ws)) return SGEMM_ERR_WORKSPACE;
     const int c_vec = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
+    int n = 0;
     rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, const_cast<void*>(ws), ws_bytes,
-                         d->sms, s);
-    g_launches.fetch_add(1, std::memory_order_relaxed);
+                         d->sms, s, &n);
+    g_launches.fetch_add(n, std::memory_order_relaxed);
     return rc;
+}
+
+int sgemm_tf32x3_query_config(int M, int N, int K, sgemm_config* out) {
+    if (out == nullptr || M <= 0 || N <= 0 || K <= 0) return SGEMM_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof(*out));
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_UNSUPPORTED;
+    const DeviceInfo* d = nullptr;
+    const int rc = device_info(dev, &d);
+    if (rc != SGEMM_OK) return rc;
+    return tf32x3_query(M, N, K, d->sms, out);
 }
 
 int sgemm_tf32x3_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb,

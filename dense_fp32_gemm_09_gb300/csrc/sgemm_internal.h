@@ -63,8 +63,10 @@ size_t tf32x3_workspace_bytes(int M, int N, int K);
 int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const float* B,
                    long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
 int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
-                    int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
-int tf32x3_tile_width(int M, int N, int sms);
+                    int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream,
+                    int* launches);
+int tf32x3_tile_width(int M, int N, int K, int sms);
+int tf32x3_query(int M, int N, int K, int sms, sgemm_config* out);
 
 
 }  // namespace sgemm

@@ -10,7 +10,8 @@
 // is dropped).  Each product of two TF32 numbers is exact in fp32 and the three
 // MMAs accumulate in fp32 in tensor memory.
 //
-// Structure (one CTA per SM, persistent over 128 x BN output tiles):
+// Structure (one CTA per SM, persistent; the same data-parallel + stream-K
+// schedule as the FFMA kernels, over 128 x BN output tiles and 32-deep k-blocks):
 //   * split_a_kernel / split_bt_kernel write Ahi, Alo (M x Kp, K-major like A)
 //     and Bhi^T, Blo^T (N x Kp, K-major: B transposed) to a workspace;
 //   * warp 0, one thread: TMA loads of the four K-major 128-byte-swizzled tiles
@@ -19,8 +20,10 @@
 //     tcgen05.mma.kind::tf32 (M = 128, N = BN, K = 8) into one of two fp32
 //     accumulators in TMEM; tcgen05.commit releases smem stages and hands a
 //     finished accumulator to the epilogue;
-//   * warps 2..5: read the accumulator with tcgen05.ld (each warp its 32 TMEM
-//     lanes = 32 rows of the tile) and store C, then free the accumulator.
+//   * warps 2..5 (2..9 for BN = 256): read the accumulator with tcgen05.ld (each
+//     warp its 32 TMEM lanes = 32 rows of the tile), then free it; a tile whose
+//     whole K range this CTA ran is stored to C, a stream-K part of a split tile
+//     to the CTA's partial slot, summed into C by sk_reduce_kernel afterwards.
 // Every mbarrier wait is bounded in time; a wait that gives up writes the
 // library's device status word (read by sgemm_device_status) and the CTA drains
 // and exits instead of hanging.
@@ -35,7 +38,9 @@
 #include <mutex>
 
 #include "sgemm_async.cuh"
+#include "sgemm_epilogue.cuh"
 #include "sgemm_internal.h"
+#include "sgemm_sched.cuh"
 
 namespace sgemm {
 namespace tc {
@@ -58,14 +63,9 @@ inline size_t align_up_floats(size_t n) { return (n + 63) / 64 * 64; }
 
 struct Params {
     CUtensorMap tm_ahi, tm_alo, tm_bhi, tm_blo;
-    float* C;
-    long long ldc;
-    int M, N, K;
-    int tiles_m, tiles_n, kblocks;
-    int c_vec;
-    int epi;
-    float alpha, beta;
-    int* status;      // device status word for waits that give up
+    // C, its epilogue, the persistent / stream-K schedule (k-blocks of BK), the
+    // partial-tile workspace and the device status word; A and B are unused.
+    GemmArgs s;
 };
 
 // ----------------------------------------------------------------------------
@@ -132,24 +132,7 @@ __host__ __device__ constexpr uint32_t tf32_idesc(int bn) {
            | (static_cast<uint32_t>(BM >> 4) << 24);   // M / 16
 }
 
-// Tile index -> origin: groups of 8 tile rows, column-major inside a group, so
-// CTAs running together share A rows and B columns in L2.
-__device__ __forceinline__ void tile_mn(const Params& p, int tile, int bn, int& m0, int& n0) {
-    const int gm = 8;
-    const int group_size = gm * p.tiles_n;
-    const int group = tile / group_size;
-    const int first_m = group * gm;
-    const int rows = min(p.tiles_m - first_m, gm);
-    const int r = tile - group * group_size;
-    m0 = (first_m + r % rows) * BM;
-    n0 = (r / rows) * bn;
-}
-
-__device__ __forceinline__ float epi_one(const Params& p, float acc, const float* c) {
-    if (p.epi == kEpiPlain) return acc;
-    if (p.epi == kEpiAlpha) return p.alpha * acc;
-    return fmaf(p.alpha, acc, p.beta * *c);
-}
+constexpr int kStageFloats = 32 * 32;   // epilogue staging block of one warp
 
 // The tensor core adds products into its fp32 accumulator with truncation, so
 // summing a long K range in one TMEM accumulator biases the result by about
@@ -157,7 +140,9 @@ __device__ __forceinline__ float epi_one(const Params& p, float acc, const float
 // chunks of KC_BLOCKS k-blocks: each chunk is accumulated in TMEM from zero, and
 // the epilogue warps add the finished chunk into an fp32 running sum in
 // registers with round-to-nearest adds.  Two TMEM chunk buffers alternate so the
-// MMAs of chunk c+1 overlap the epilogue's read of chunk c.
+// MMAs of chunk c+1 overlap the epilogue's read of chunk c.  Chunk boundaries
+// are the multiples of KC_BLOCKS k-blocks (and the ends of a CTA's part of a
+// tile), so a tile computed whole is chunked the same way under any schedule.
 template <int BN, int STAGES, int KC_BLOCKS>
 __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
     tf32x3_kernel(const __grid_constant__ Params p) {
@@ -180,11 +165,15 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t smem0 = su32(smem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles = p.tiles_m * p.tiles_n;
-    const int chunks = (p.kblocks + KC_BLOCKS - 1) / KC_BLOCKS;
+    const GemmArgs& a = p.s;
+    // The CTA's work list lives in shared memory: the epilogue warps need their
+    // registers for the 128-column running sums.
+    __shared__ CtaWork w_s;
+    const CtaWork& w = w_s;
     volatile int* abort_flag = &abort_s;
 
     if (threadIdx.x == 0) {
+        w_s = make_work(a, blockIdx.x);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(su32(&full_bar[s]), 1);
             mbar_init(su32(&empty_bar[s]), 1);
@@ -218,27 +207,31 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
             bool issued[STAGES];
             for (int s = 0; s < STAGES; ++s) issued[s] = false;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
-                int m0, n0;
-                tile_mn(p, tile, BN, m0, n0);
-                for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!async::mbar_wait(su32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = su32(&full_bar[stage]);
-                    const uint32_t base = smem0 + stage * STAGE_BYTES;
-                    mbar_expect_tx(fb, STAGE_BYTES);
-                    tma_load_2d(base, &p.tm_ahi, kb * BK, m0, fb);
-                    tma_load_2d(base + A_BYTES, &p.tm_alo, kb * BK, m0, fb);
-                    tma_load_2d(base + 2 * A_BYTES, &p.tm_bhi, kb * BK, n0, fb);
-                    tma_load_2d(base + 2 * A_BYTES + B_BYTES, &p.tm_blo, kb * BK, n0, fb);
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+            int m0 = 0, n0 = 0, tile = -1;
+            Cursor cur;
+            cur.seek(w, 0);
+            for (; cur.c < w.total; cur.advance(w)) {
+                if (cur.tile != tile) {
+                    tile = cur.tile;
+                    tile_origin(a, tile, BM, BN, m0, n0);
+                }
+                if (!async::mbar_wait(su32(&empty_bar[stage]), phase ^ 1u, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = su32(&full_bar[stage]);
+                const uint32_t base = smem0 + stage * STAGE_BYTES;
+                const int k0 = cur.kt * BK;
+                mbar_expect_tx(fb, STAGE_BYTES);
+                tma_load_2d(base, &p.tm_ahi, k0, m0, fb);
+                tma_load_2d(base + A_BYTES, &p.tm_alo, k0, m0, fb);
+                tma_load_2d(base + 2 * A_BYTES, &p.tm_bhi, k0, n0, fb);
+                tma_load_2d(base + 2 * A_BYTES + B_BYTES, &p.tm_blo, k0, n0, fb);
+                issued[stage] = true;
+                issued_phase[stage] = phase;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
             if (!ok) {
@@ -257,67 +250,76 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
             int buf = 0;
             uint32_t buf_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
-                for (int c = 0; ok && c < chunks; ++c) {
-                    if (!async::mbar_wait(su32(&tempty_bar[buf]), buf_phase ^ 1u, abort_flag, p.status)) {
+            Cursor cur;
+            cur.seek(w, 0);
+            while (ok && cur.c < w.total) {
+                // one chunk: k-blocks up to the next multiple of KC_BLOCKS or the end
+                // of this CTA's part of the tile
+                if (!async::mbar_wait(su32(&tempty_bar[buf]), buf_phase ^ 1u, abort_flag, a.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                bool first = true, end_chunk = false;
+                while (!end_chunk) {
+                    if (!async::mbar_wait(su32(&full_bar[stage]), phase, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                    const int kb_end = min(p.kblocks, (c + 1) * KC_BLOCKS);
-                    for (int kb = c * KC_BLOCKS; kb < kb_end; ++kb) {
-                        if (!async::mbar_wait(su32(&full_bar[stage]), phase, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t base = smem0 + stage * STAGE_BYTES;
-                        const bool first = (kb == c * KC_BLOCKS);
+                    const uint32_t base = smem0 + stage * STAGE_BYTES;
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            const uint32_t off = k * UMMA_K * 4;
-                            const uint64_t ahi = sw128_kmajor_desc(base + off);
-                            const uint64_t alo = sw128_kmajor_desc(base + A_BYTES + off);
-                            const uint64_t bhi = sw128_kmajor_desc(base + 2 * A_BYTES + off);
-                            const uint64_t blo =
-                                sw128_kmajor_desc(base + 2 * A_BYTES + B_BYTES + off);
-                            umma_tf32(d_tmem, alo, bhi, idesc, (first && k == 0) ? 0u : 1u);
-                            umma_tf32(d_tmem, ahi, blo, idesc, 1u);
-                            umma_tf32(d_tmem, ahi, bhi, idesc, 1u);
-                        }
-                        umma_commit(su32(&empty_bar[stage]));
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        const uint32_t off = k * UMMA_K * 4;
+                        const uint64_t ahi = sw128_kmajor_desc(base + off);
+                        const uint64_t alo = sw128_kmajor_desc(base + A_BYTES + off);
+                        const uint64_t bhi = sw128_kmajor_desc(base + 2 * A_BYTES + off);
+                        const uint64_t blo = sw128_kmajor_desc(base + 2 * A_BYTES + B_BYTES + off);
+                        umma_tf32(d_tmem, alo, bhi, idesc, (first && k == 0) ? 0u : 1u);
+                        umma_tf32(d_tmem, ahi, blo, idesc, 1u);
+                        umma_tf32(d_tmem, ahi, bhi, idesc, 1u);
                     }
-                    if (!ok) break;
-                    umma_commit(su32(&tfull_bar[buf]));
-                    buf ^= 1;
-                    if (buf == 0) buf_phase ^= 1u;
+                    umma_commit(su32(&empty_bar[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                    first = false;
+                    end_chunk = (cur.kt + 1 == cur.kt_end) || ((cur.kt + 1) % KC_BLOCKS == 0);
+                    cur.advance(w);
                 }
+                if (!ok) break;
+                umma_commit(su32(&tfull_bar[buf]));
+                buf ^= 1;
+                if (buf == 0) buf_phase ^= 1u;
             }
         }
     } else {
-        // ---------------- epilogue: TMEM chunks -> fp32 sums -> C ----------------
+        // ---------------- epilogue: TMEM chunks -> fp32 sums -> C or a partial ----------------
         // Warp w may read TMEM lanes [32 (w % 4), +32) = 32 rows of the tile; the
         // epilogue warps come in groups of four, group g owning columns
         // [128 g, 128 g + 128).
         constexpr int EC = 128;            // accumulator columns per epilogue warp
         const int q = warp & 3;
         const int col0 = EC * ((warp - 2) / 4);
+        float* const stg =
+            reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES) + (warp - 2) * kStageFloats;
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+        Cursor cur;
+        cur.seek(w, 0);
+        while (ok && cur.c < w.total) {
+            const int tile = cur.tile, kt_begin = cur.kt_begin, kt_end = cur.kt_end;
             int m0, n0;
-            tile_mn(p, tile, BN, m0, n0);
+            tile_origin(a, tile, BM, BN, m0, n0);
             float sum[EC];
 #pragma unroll
             for (int i = 0; i < EC; ++i) sum[i] = 0.0f;
-            for (int c = 0; c < chunks; ++c) {
-                if (!async::mbar_wait(su32(&tfull_bar[buf]), buf_phase, abort_flag, p.status)) {
+            for (;;) {
+                const int ce = min(kt_end, (cur.kt / KC_BLOCKS + 1) * KC_BLOCKS);
+                if (!async::mbar_wait(su32(&tfull_bar[buf]), buf_phase, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
@@ -337,34 +339,39 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
                 if (lane == 0) mbar_arrive(su32(&tempty_bar[buf]));
                 buf ^= 1;
                 if (buf == 0) buf_phase ^= 1u;
+                cur.seek(w, cur.c + (ce - cur.kt));
+                if (ce == kt_end) break;
             }
             if (!ok) break;
-            const int row = m0 + 32 * q + lane;
-            if (row < p.M) {
-                float* crow = p.C + static_cast<long long>(row) * p.ldc;
+            // Stores go through a 32 x 32 staging block per warp (16-byte chunks
+            // XOR-swizzled by row, so both the row-wise writes and the column-wise
+            // reads are conflict-free): each store instruction then covers four
+            // whole 128-byte row segments instead of 32 scattered 16-byte pieces.
+            const bool partial = kt_begin != 0 || kt_end != a.KT;
+            float* P = partial ? a.ws_partial + (static_cast<long long>(w.g) * 2 +
+                                                 sk_slot(w, tile - w.dp_tiles)) * (BM * BN)
+                               : nullptr;
 #pragma unroll
-                for (int j = 0; j < EC / 32; ++j) {
-                    const int c0 = n0 + col0 + 32 * j;
-                    if (p.c_vec && c0 + 31 < p.N) {
+            for (int j = 0; j < EC / 32; ++j) {
+                __syncwarp();
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            float4 o = make_float4(sum[32 * j + 4 * u], sum[32 * j + 4 * u + 1],
-                                                   sum[32 * j + 4 * u + 2],
-                                                   sum[32 * j + 4 * u + 3]);
-                            if (p.epi != kEpiPlain) {
-                                const float* cp = crow + c0 + 4 * u;
-                                o.x = epi_one(p, o.x, cp + 0);
-                                o.y = epi_one(p, o.y, cp + 1);
-                                o.z = epi_one(p, o.z, cp + 2);
-                                o.w = epi_one(p, o.w, cp + 3);
-                            }
-                            *reinterpret_cast<float4*>(crow + c0 + 4 * u) = o;
-                        }
-                    } else {
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) * 4)) =
+                        make_float4(sum[32 * j + 4 * u], sum[32 * j + 4 * u + 1],
+                                    sum[32 * j + 4 * u + 2], sum[32 * j + 4 * u + 3]);
+                __syncwarp();
+                const int c4 = lane & 7;
 #pragma unroll
-                        for (int u = 0; u < 32; ++u)
-                            if (c0 + u < p.N)
-                                crow[c0 + u] = epi_one(p, sum[32 * j + u], crow + c0 + u);
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = 4 * i + (lane >> 3);            // row in the block
+                    const float4 v =
+                        *reinterpret_cast<const float4*>(stg + rr * 32 + ((c4 ^ (rr & 7)) * 4));
+                    const int tr = 32 * q + rr;                    // row of the tile
+                    const int tc = col0 + 32 * j + 4 * c4;         // column of the tile
+                    if (partial) {
+                        __stcg(reinterpret_cast<float4*>(P + tr * BN + tc), v);
+                    } else if (m0 + tr < a.M) {
+                        store_c4(a, a.C + static_cast<long long>(m0 + tr) * a.ldc, n0 + tc, v);
                     }
                 }
             }
@@ -373,6 +380,8 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
 
     tc_fence_before();
     __syncthreads();
+    // Every store of this CTA is issued: a dependent reduction may start.
+    asm volatile("griddepcontrol.launch_dependents;");
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -477,7 +486,8 @@ struct Variant {
     static constexpr int kStages = BN == 256 ? 2 : 3;
     static constexpr int kThreads = tf32x3_threads(BN);
     static constexpr size_t kSmem =
-        static_cast<size_t>(kStages) * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024;
+        static_cast<size_t>(kStages) * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024 +
+        static_cast<size_t>(4 * (BN / 128)) * kStageFloats * 4;   // + epilogue staging
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -515,15 +525,90 @@ size_t region_floats(long long rows, int Kp) {
 
 }  // namespace tc
 
+namespace {
+
+int current_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
+// The schedule of one multiply (one CTA per SM) for tile width bn.
+GemmArgs tf32x3_plan(int M, int N, int K, int bn, int sms, int schedule, SchedSizes* z) {
+    GemmArgs s{};
+    s.M = M;
+    s.N = N;
+    s.K = K;
+    *z = plan_schedule(s, tc::BM, bn, tc::BK, sms, 1, schedule);
+    return s;
+}
+
+struct TcChoice {
+    int bn, schedule;
+};
+
+// Tile width (128 or 256) and schedule (1: data-parallel only, 0: stream-K on a
+// partial last wave or when tiles are fewer than SMs) with the smaller estimated
+// time: the k-blocks of the busiest CTA, a 256-wide k-block counting 1.9
+// 128-wide ones (each MMA re-reads A for twice the columns, about 5 % faster per
+// column), plus, when tiles are split, 8 k-blocks for the reduction launch and
+// 0.12 per 128-column split tile for writing and re-reading its partials
+// (fitted to measured times at 1024^3 .. 8192^3 and the ragged and tall shapes).
+// SGEMM_TF32X3_BN and SGEMM_TF32X3_SCHEDULE (0 auto, 1 data-parallel, 2
+// stream-K whenever possible) override it for tests and tuning.
+TcChoice tf32x3_choice(int M, int N, int K, int sms) {
+    int force_bn = 0, force_sched = -1;
+    if (const char* env = std::getenv("SGEMM_TF32X3_BN")) {
+        const int bn = std::atoi(env);
+        if (bn == 128 || bn == 256) force_bn = bn;
+    }
+    if (const char* env = std::getenv("SGEMM_TF32X3_SCHEDULE")) {
+        const int v = std::atoi(env);
+        if (v >= 0 && v <= 2) force_sched = v;
+    }
+    TcChoice best{256, 1};
+    double best_t = -1.0;
+    for (int bn : {256, 128}) {
+        if (force_bn && bn != force_bn) continue;
+        for (int sched : {1, 0, 2}) {
+            if (force_sched >= 0 ? sched != force_sched : sched == 2) continue;
+            SchedSizes z;
+            const GemmArgs s = tf32x3_plan(M, N, K, bn, sms, sched, &z);
+            const long long dp_per = (static_cast<long long>(s.dp_tiles) + s.grid - 1) / s.grid;
+            const long long sk_per = (s.sk_iters + s.grid - 1) / s.grid;
+            const double split_cost = s.sk_tiles > 0 ? 8.0 + 0.12 * s.sk_tiles * (bn / 128) : 0.0;
+            const double t =
+                static_cast<double>(dp_per * s.KT + sk_per) * (bn == 256 ? 1.9 : 1.0) + split_cost;
+            if (best_t < 0.0 || t < best_t) {
+                best_t = t;
+                best = TcChoice{bn, sched};
+            }
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
 size_t tf32x3_workspace_bytes(int M, int N, int K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
     const int Kp = (K + 3) / 4 * 4;
-    return 4 * (2 * tc::region_floats(M, Kp) + 2 * tc::region_floats(N, Kp));
+    const int sms = current_sms();
+    size_t partial = 0;
+    if (sms > 0) {
+        SchedSizes z;
+        const TcChoice c = tf32x3_choice(M, N, K, sms);
+        tf32x3_plan(M, N, K, c.bn, sms, c.schedule, &z);
+        partial = z.partial_bytes;
+    }
+    return 4 * (2 * tc::region_floats(M, Kp) + 2 * tc::region_floats(N, Kp)) + partial;
 }
 
 namespace {
 struct WsLayout {
-    float *ahi, *alo, *bhi, *blo;
+    float *ahi, *alo, *bhi, *blo, *partial;
 };
 WsLayout ws_layout(void* ws, int M, int N, int Kp) {
     WsLayout L;
@@ -531,6 +616,7 @@ WsLayout ws_layout(void* ws, int M, int N, int Kp) {
     L.alo = L.ahi + tc::region_floats(M, Kp);
     L.bhi = L.alo + tc::region_floats(M, Kp);
     L.blo = L.bhi + tc::region_floats(N, Kp);
+    L.partial = L.blo + tc::region_floats(N, Kp);
     return L;
 }
 }  // namespace
@@ -564,15 +650,10 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
 
 namespace {
 
-// Fraction of the last wave of `tiles` tiles over `ctas` CTAs that does work.
-double wave_efficiency(long long tiles, int ctas) {
-    const long long waves = (tiles + ctas - 1) / ctas;
-    return static_cast<double>(tiles) / static_cast<double>(waves * ctas);
-}
-
 template <int BN>
 int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
-                   int c_vec, const WsLayout& L, int Kp, int sms, cudaStream_t stream) {
+                   int c_vec, const WsLayout& L, size_t partial_bytes, int Kp, int sms,
+                   int schedule, cudaStream_t stream, int* launches) {
     using namespace tc;
     using V = Variant<BN>;
     static std::once_flag attr_once;
@@ -594,57 +675,90 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
         set_last_error_message("tf32x3: cuTensorMapEncodeTiled failed");
         return SGEMM_ERR_LAUNCH;
     }
-    p.C = C;
-    p.ldc = ldc;
-    p.M = M;
-    p.N = N;
-    p.K = K;
-    p.tiles_m = (M + BM - 1) / BM;
-    p.tiles_n = (N + BN - 1) / BN;
-    p.kblocks = (K + BK - 1) / BK;
-    p.c_vec = c_vec;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.epi = (beta != 0.0f) ? kEpiAlphaBeta : (alpha != 1.0f ? kEpiAlpha : kEpiPlain);
-    p.status = status_word_ptr();
-    const int tiles = p.tiles_m * p.tiles_n;
-    const int grid = std::min(tiles, sms);
-    tf32x3_kernel<BN, V::kStages, kChunkBlocks><<<grid, V::kThreads, V::kSmem, stream>>>(p);
+    SchedSizes z;
+    p.s = tf32x3_plan(M, N, K, BN, sms, schedule, &z);
+    if (z.partial_bytes > partial_bytes) {
+        set_last_error_message("tf32x3: workspace too small for the split tiles");
+        return SGEMM_ERR_WORKSPACE;
+    }
+    p.s.C = C;
+    p.s.ldc = ldc;
+    p.s.c_vec = c_vec;
+    p.s.alpha = alpha;
+    p.s.beta = beta;
+    p.s.epi = (beta != 0.0f) ? kEpiAlphaBeta : (alpha != 1.0f ? kEpiAlpha : kEpiPlain);
+    p.s.ws_partial = L.partial;
+    p.s.status = status_word_ptr();
+    tf32x3_kernel<BN, V::kStages, kChunkBlocks><<<p.s.grid, V::kThreads, V::kSmem, stream>>>(p);
+    *launches = 1;
     if (cudaGetLastError() != cudaSuccess) {
         set_last_error_message("tf32x3: GEMM kernel failed to launch");
         return SGEMM_ERR_LAUNCH;
+    }
+    if (p.s.sk_tiles > 0) {
+        if (launch_sk_reduce(p.s, BM, BN, sms, stream) != cudaSuccess) {
+            set_last_error_message("tf32x3: split-tile reduction failed to launch");
+            return SGEMM_ERR_LAUNCH;
+        }
+        *launches = 2;
     }
     return SGEMM_OK;
 }
 
 }  // namespace
 
-int tf32x3_tile_width(int M, int N, int sms) {
-    if (const char* force = std::getenv("SGEMM_TF32X3_BN")) {
-        const int bn = std::atoi(force);
-        if (bn == 128 || bn == 256) return bn;
-    }
-    // 256-wide tiles run about 5 % faster per tile (each MMA re-reads A for twice
-    // the columns) but quantise into fewer, larger waves and pad narrow C more:
-    // pick the better expected efficiency.
-    const long long tm = (M + tc::BM - 1) / tc::BM;
-    const long long t128 = (N + 127) / 128, t256 = (N + 255) / 256;
-    const double e128 = wave_efficiency(tm * t128, sms) * N / (128.0 * t128);
-    const double e256 = wave_efficiency(tm * t256, sms) * N / (256.0 * t256);
-    return e256 * 1.05 > e128 ? 256 : 128;
+int tf32x3_tile_width(int M, int N, int K, int sms) {
+    return tf32x3_choice(M, N, K, sms).bn;
+}
+
+int tf32x3_query(int M, int N, int K, int sms, sgemm_config* out) {
+    const TcChoice c = tf32x3_choice(M, N, K, sms);
+    const int bn = c.bn;
+    SchedSizes z;
+    const GemmArgs s = tf32x3_plan(M, N, K, bn, sms, c.schedule, &z);
+    const bool wide = bn == 256;
+    out->bm = tc::BM;
+    out->bn = bn;
+    out->bk = tc::BK;
+    out->wm = 32;
+    out->wn = 128;
+    out->tm = 1;
+    out->tn = 128;
+    out->stages = wide ? tc::Variant<256>::kStages : tc::Variant<128>::kStages;
+    out->threads = tc::tf32x3_threads(bn);
+    out->smem_bytes = static_cast<int>(wide ? tc::Variant<256>::kSmem : tc::Variant<128>::kSmem);
+    out->split_k = z.split;
+    out->kernel_id = -1;
+    out->vec = 4;
+    out->grid = s.grid;
+    out->tiles = s.tiles_m * s.tiles_n;
+    out->sk_tiles = s.sk_tiles;
+    out->ctas_per_sm = 1;
+    out->fma2 = 0;
+    out->packed = 0;
+    return SGEMM_OK;
 }
 
 int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
-                    int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream) {
-    if (ws == nullptr || ws_bytes < tf32x3_workspace_bytes(M, N, K)) {
+                    int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream,
+                    int* launches) {
+    *launches = 0;
+    const size_t need = tf32x3_workspace_bytes(M, N, K);
+    if (ws == nullptr || ws_bytes < need) {
         set_last_error_message("tf32x3: workspace too small");
         return SGEMM_ERR_WORKSPACE;
     }
     const int Kp = (K + 3) / 4 * 4;
     const WsLayout L = ws_layout(ws, M, N, Kp);
-    if (tf32x3_tile_width(M, N, sms) == 256)
-        return launch_variant<256>(M, N, K, alpha, beta, C, ldc, c_vec, L, Kp, sms, stream);
-    return launch_variant<128>(M, N, K, alpha, beta, C, ldc, c_vec, L, Kp, sms, stream);
+    const size_t partial_bytes =
+        ws_bytes - static_cast<size_t>(reinterpret_cast<char*>(L.partial) -
+                                       static_cast<char*>(ws));
+    const TcChoice c = tf32x3_choice(M, N, K, sms);
+    if (c.bn == 256)
+        return launch_variant<256>(M, N, K, alpha, beta, C, ldc, c_vec, L, partial_bytes, Kp,
+                                   sms, c.schedule, stream, launches);
+    return launch_variant<128>(M, N, K, alpha, beta, C, ldc, c_vec, L, partial_bytes, Kp, sms,
+                               c.schedule, stream, launches);
 }
 
 }  // namespace sgemm

@@ -215,6 +215,15 @@ SGEMM_API int sgemm_tf32x3_run_ex(int M, int N, int K, float alpha, const float*
                                   void* ws, size_t ws_bytes, sgemm_stream_t stream);
 SGEMM_API int sgemm_tf32x3_workspace_size(int M, int N, int K, size_t* out_bytes);
 
+/* The configuration sgemm_tf32x3_run_ex would use for M x N x K on the current
+ * device: bm x bn output tiles (bn 128 or 256, chosen per problem), bk = 32-deep
+ * k-blocks, stages, threads, shared memory, the persistent grid, the tile count,
+ * the tiles split by k-blocks over several CTAs (sk_tiles; their partials are
+ * summed by a second, deterministic kernel) and the most CTAs sharing one
+ * (split_k).  kernel_id is -1 (not a tile-table entry).  Errors:
+ * SGEMM_ERR_INVALID_ARG for a null `out` or a non-positive size. */
+SGEMM_API int sgemm_tf32x3_query_config(int M, int N, int K, sgemm_config* out);
+
 /* The two steps of sgemm_tf32x3_run_ex, for callers that reuse operands or time
  * the steps apart.  _prepare writes the TF32 hi/lo parts of A (M x K) and the
  * transposed parts of B (K x N) into `ws` (caller-owned, 16-byte aligned, at

@@ -31,13 +31,18 @@ def run(torch, A, B, C=None, alpha=1.0, beta=0.0, lda=None, ldb=None):
     return C
 
 
-@pytest.fixture(params=["auto", "128", "256"])
+@pytest.fixture(params=["auto", "128/dp", "256/dp", "128/sk", "256/sk"])
 def tile_width(request, monkeypatch):
-    """Run with the library's choice of tile width, then forced to each width."""
+    """Run with the library's choice of tile width and schedule, then forced to each
+    width with data-parallel tiles only (dp) and with stream-K on every partial
+    wave (sk)."""
     if request.param == "auto":
         monkeypatch.delenv("SGEMM_TF32X3_BN", raising=False)
+        monkeypatch.delenv("SGEMM_TF32X3_SCHEDULE", raising=False)
     else:
-        monkeypatch.setenv("SGEMM_TF32X3_BN", request.param)
+        bn, sched = request.param.split("/")
+        monkeypatch.setenv("SGEMM_TF32X3_BN", bn)
+        monkeypatch.setenv("SGEMM_TF32X3_SCHEDULE", "1" if sched == "dp" else "2")
     return request.param
 
 
@@ -128,3 +133,28 @@ def test_caller_workspace_and_sizes(cuda):
                                    0.0, C.data_ptr(), 200, ws.data_ptr(), need - 4, s) == -6
     torch.cuda.synchronize()
     assert lib.sgemm_device_status() == 0
+
+
+@pytest.mark.parametrize("sched", ["0", "2"])
+def test_stream_k_deterministic(cuda, monkeypatch, sched):
+    """Split tiles are summed in a fixed order: two runs agree bit for bit."""
+    torch = cuda
+    monkeypatch.setenv("SGEMM_TF32X3_SCHEDULE", sched)
+    A, B = random_pair(1000, 700, 2000, seed=9)
+    dA, dB = A.cuda(), B.cuda()
+    C1 = run(torch, dA, dB).clone()
+    C2 = run(torch, dA, dB)
+    assert torch.equal(C1, C2)
+
+
+def test_stream_k_scaled_into_split_tiles(cuda, oracle_mod, monkeypatch):
+    """alpha/beta on tiles finished by the split-tile reduction."""
+    torch = cuda
+    monkeypatch.setenv("SGEMM_TF32X3_SCHEDULE", "2")
+    M, N, K = 384, 640, 1536
+    A, B = random_pair(M, N, K, seed=10)
+    C0 = torch.randn(M, N, generator=torch.Generator().manual_seed(3))
+    C = run(torch, A.cuda(), B.cuda(), C=C0.cuda(), alpha=0.5, beta=-1.25)
+    ref = oracle_mod.gemm_f64_ex(0.5, A.numpy(), B.numpy(), -1.25, C0.numpy())
+    err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+    assert err <= 0.5 * tol(A, B) + 1e-5 * 1.25 * float(C0.abs().max())
