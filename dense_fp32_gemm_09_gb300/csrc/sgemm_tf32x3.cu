@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
     constexpr uint32_t B_BYTES = BN * BK * 4;
     constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     constexpr uint32_t TMEM_COLS = 2 * BN;   // two chunk accumulators
+    constexpr bool STAGED = BN == 128;       // epilogue stores through shared memory
     static_assert(BN == 128 || BN == 256, "BN");
     static_assert(TMEM_COLS == 64 || TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512,
                   "TMEM allocation must be a power of two");
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
         const int col0 = EC * ((warp - 2) / 4);
         float* const stg =
             reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES) + (warp - 2) * kStageFloats;
+        (void)stg;
         int buf = 0;
         uint32_t buf_phase = 0;
         bool ok = true;
@@ -343,14 +345,30 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
                 if (ce == kt_end) break;
             }
             if (!ok) break;
-            // Stores go through a 32 x 32 staging block per warp (16-byte chunks
-            // XOR-swizzled by row, so both the row-wise writes and the column-wise
-            // reads are conflict-free): each store instruction then covers four
-            // whole 128-byte row segments instead of 32 scattered 16-byte pieces.
             const bool partial = kt_begin != 0 || kt_end != a.KT;
             float* P = partial ? a.ws_partial + (static_cast<long long>(w.g) * 2 +
                                                  sk_slot(w, tile - w.dp_tiles)) * (BM * BN)
                                : nullptr;
+            if constexpr (!STAGED) {
+                // Each lane stores its own row (the 256-wide variant has neither the
+                // registers nor the shared memory for the staging block).
+                const int tr = 32 * q + lane;
+#pragma unroll
+                for (int u = 0; u < EC / 4; ++u) {
+                    const float4 v = make_float4(sum[4 * u], sum[4 * u + 1], sum[4 * u + 2],
+                                                 sum[4 * u + 3]);
+                    const int tc = col0 + 4 * u;
+                    if (partial)
+                        __stcg(reinterpret_cast<float4*>(P + tr * BN + tc), v);
+                    else if (m0 + tr < a.M)
+                        store_c4(a, a.C + static_cast<long long>(m0 + tr) * a.ldc, n0 + tc, v);
+                }
+                continue;
+            }
+            // Stores go through a 32 x 32 staging block per warp (16-byte chunks
+            // XOR-swizzled by row, so both the row-wise writes and the column-wise
+            // reads are conflict-free): each store instruction then covers four
+            // whole 128-byte row segments instead of 32 scattered 16-byte pieces.
 #pragma unroll
             for (int j = 0; j < EC / 32; ++j) {
                 __syncwarp();
@@ -487,7 +505,7 @@ struct Variant {
     static constexpr int kThreads = tf32x3_threads(BN);
     static constexpr size_t kSmem =
         static_cast<size_t>(kStages) * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024 +
-        static_cast<size_t>(4 * (BN / 128)) * kStageFloats * 4;   // + epilogue staging
+        (BN == 128 ? static_cast<size_t>(4) * kStageFloats * 4 : 0);   // + epilogue staging
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -553,9 +571,11 @@ struct TcChoice {
 // partial last wave or when tiles are fewer than SMs) with the smaller estimated
 // time: the k-blocks of the busiest CTA, a 256-wide k-block counting 1.9
 // 128-wide ones (each MMA re-reads A for twice the columns, about 5 % faster per
-// column), plus, when tiles are split, 8 k-blocks for the reduction launch and
-// 0.12 per 128-column split tile for writing and re-reading its partials
-// (fitted to measured times at 1024^3 .. 8192^3 and the ragged and tall shapes).
+// column), plus, when tiles are split, 8 k-blocks for the reduction launch and,
+// per 128 columns of split tile, 0.12 (128-wide: staged, coalesced partial
+// stores) or 0.3 (256-wide: a row per lane) for writing and re-reading its
+// partials (fitted to measured times at 1024^3 .. 8192^3 and the ragged and
+// tall shapes).
 // SGEMM_TF32X3_BN and SGEMM_TF32X3_SCHEDULE (0 auto, 1 data-parallel, 2
 // stream-K whenever possible) override it for tests and tuning.
 TcChoice tf32x3_choice(int M, int N, int K, int sms) {
@@ -578,7 +598,8 @@ TcChoice tf32x3_choice(int M, int N, int K, int sms) {
             const GemmArgs s = tf32x3_plan(M, N, K, bn, sms, sched, &z);
             const long long dp_per = (static_cast<long long>(s.dp_tiles) + s.grid - 1) / s.grid;
             const long long sk_per = (s.sk_iters + s.grid - 1) / s.grid;
-            const double split_cost = s.sk_tiles > 0 ? 8.0 + 0.12 * s.sk_tiles * (bn / 128) : 0.0;
+            const double split_cost =
+                s.sk_tiles > 0 ? 8.0 + (bn == 256 ? 0.3 : 0.12) * s.sk_tiles * (bn / 128) : 0.0;
             const double t =
                 static_cast<double>(dp_per * s.KT + sk_per) * (bn == 256 ? 1.9 : 1.0) + split_cost;
             if (best_t < 0.0 || t < best_t) {
