@@ -376,18 +376,50 @@ int host_pipe(HostPipe** out) {
     return SGEMM_OK;
 }
 
-// Row panels for the host-buffer entry.  SGEMM_HOST_PANELS overrides (tuning).
-int host_panel_rows(int M, int N, int K) {
-    int panels = 1;
-    if (const char* env = std::getenv("SGEMM_HOST_PANELS")) {
-        panels = std::atoi(env);
-    } else {
-        const double macs = static_cast<double>(M) * N * K;
-        panels = macs >= 4.0e9 ? 4 : (macs >= 5.0e8 ? 2 : 1);
+// Row panels for the host-buffer entry: fills rows[] (multiples of 128 but the
+// last) and returns their number.  Large problems: 25 % of the rows (computed in
+// k-chunks as their inputs arrive), then 65 % in one efficient product, then a
+// last 10 % whose copy back is the only exposed tail (measured best of several
+// splits at 4096^3 and 8192^3); mid-size problems: two halves.  SGEMM_HOST_PANELS
+// (a count of equal panels) or SGEMM_HOST_SPLIT (percentages of M, e.g.
+// "25,65,10") override it (tuning).
+int host_panels(int M, int N, int K, int (&rows)[kMaxHostPanels]) {
+    int pct[kMaxHostPanels];
+    int n_pct = 0;
+    if (const char* env = std::getenv("SGEMM_HOST_SPLIT")) {
+        for (const char* c = env; *c && n_pct < kMaxHostPanels;) {
+            const int v = std::atoi(c);
+            if (v > 0) pct[n_pct++] = v;
+            while (*c && *c != ',') ++c;
+            if (*c == ',') ++c;
+        }
     }
-    panels = std::max(1, std::min(panels, kMaxHostPanels));
-    const int rows = (M + panels - 1) / panels;
-    return std::max(128, (rows + 127) / 128 * 128);
+    if (n_pct == 0) {
+        const double macs = static_cast<double>(M) * N * K;
+        if (const char* env = std::getenv("SGEMM_HOST_PANELS")) {
+            n_pct = std::max(1, std::min(std::atoi(env), kMaxHostPanels));
+            for (int i = 0; i < n_pct; ++i) pct[i] = 1;
+        } else if (macs >= 4.0e9) {
+            n_pct = 3;
+            pct[0] = 25;
+            pct[1] = 65;
+            pct[2] = 10;
+        } else {
+            n_pct = macs >= 5.0e8 ? 2 : 1;
+            for (int i = 0; i < n_pct; ++i) pct[i] = 1;
+        }
+    }
+    int total = 0;
+    for (int i = 0; i < n_pct; ++i) total += pct[i];
+    int n = 0, done = 0;
+    for (int i = 0; i < n_pct && done < M; ++i) {
+        int r = static_cast<int>(static_cast<long long>(M) * pct[i] / total);
+        r = std::max(128, (r + 127) / 128 * 128);
+        if (i == n_pct - 1 || done + r > M) r = M - done;
+        rows[n++] = r;
+        done += r;
+    }
+    return n;
 }
 
 // Depth of the k-chunks in which the first row panel is computed, so that its
@@ -912,13 +944,14 @@ int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* h
         return SGEMM_ERR_LAUNCH;
     }
     const char* failed = nullptr;
-    const int rows = host_panel_rows(M, N, K);
+    int rows[kMaxHostPanels];
+    const int n_panels = host_panels(M, N, K, rows);
     const int kc = host_kchunk(M, N, K);
     const size_t fa = sizeof(float) * lda, fb = sizeof(float) * ldb, fc = sizeof(float) * ldc;
     if (K > 0) {
         // Copy order: the first panel's A and B k-chunk by k-chunk (all of B
         // once the last chunk is in), then the other panels' A.
-        const int mr0 = std::min(rows, M);
+        const int mr0 = rows[0];
         for (int c = 0, k0 = 0; k0 < K && e == cudaSuccess; ++c, k0 += kc) {
             const int kw = std::min(kc, K - k0);
             const long long ob = static_cast<long long>(k0) * ldb;
@@ -929,16 +962,17 @@ int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* h
                                       cudaMemcpyHostToDevice, hp->h2d);
             if (e == cudaSuccess) e = cudaEventRecord(hp->k_in[c], hp->h2d);
         }
-        for (int p = 1, r0 = rows; r0 < M && e == cudaSuccess; ++p, r0 += rows) {
+        for (int p = 1, r0 = rows[0]; p < n_panels && e == cudaSuccess; r0 += rows[p++]) {
             const long long oa = static_cast<long long>(r0) * lda;
-            e = cudaMemcpy2DAsync(dA + oa, fa, hA + oa, fa, sizeof(float) * K,
-                                  std::min(rows, M - r0), cudaMemcpyHostToDevice, hp->h2d);
+            e = cudaMemcpy2DAsync(dA + oa, fa, hA + oa, fa, sizeof(float) * K, rows[p],
+                                  cudaMemcpyHostToDevice, hp->h2d);
             if (e == cudaSuccess) e = cudaEventRecord(hp->a_in[p], hp->h2d);
         }
         if (e != cudaSuccess) failed = "host-to-device copy";
     }
-    for (int p = 0, r0 = 0; r0 < M && failed == nullptr && rc == SGEMM_OK; ++p, r0 += rows) {
-        const int mr = std::min(rows, M - r0);
+    for (int p = 0, r0 = 0; p < n_panels && failed == nullptr && rc == SGEMM_OK;
+         r0 += rows[p++]) {
+        const int mr = rows[p];
         const long long oa = static_cast<long long>(r0) * lda;
         const long long oc = static_cast<long long>(r0) * ldc;
         const sgemm_stream_t comp = reinterpret_cast<sgemm_stream_t>(hp->comp);
