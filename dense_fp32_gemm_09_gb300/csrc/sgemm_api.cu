@@ -1075,7 +1075,7 @@ int sgemm_tf32x3_run_ex(int M, int N, int K, float alpha, const float* A, int ld
     }
     const int c_vec = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
     rc = tf32x3_prepare(M, N, K, A, lda, B, ldb, ws, ws_bytes, d->sms, s);
-    g_launches.fetch_add(2, std::memory_order_relaxed);
+    g_launches.fetch_add(1, std::memory_order_relaxed);   // split_kernel
     if (rc != SGEMM_OK) return rc;
     int n = 0;
     rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, ws, ws_bytes, d->sms, s, &n);
@@ -1096,7 +1096,7 @@ int sgemm_tf32x3_prepare(int M, int N, int K, const float* A, int lda, const flo
     if (!aligned16(ws)) return SGEMM_ERR_WORKSPACE;
     rc = tf32x3_prepare(M, N, K, A, lda, B, ldb, ws, ws_bytes,
                         d->sms, reinterpret_cast<cudaStream_t>(stream));
-    g_launches.fetch_add(2, std::memory_order_relaxed);
+    g_launches.fetch_add(1, std::memory_order_relaxed);   // split_kernel
     return rc;
 }
 

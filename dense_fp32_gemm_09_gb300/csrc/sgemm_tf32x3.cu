@@ -12,8 +12,8 @@
 //
 // Structure (one CTA per SM, persistent; the same data-parallel + stream-K
 // schedule as the FFMA kernels, over 128 x BN output tiles and 32-deep k-blocks):
-//   * split_a_kernel / split_bt_kernel write Ahi, Alo (M x Kp, K-major like A)
-//     and Bhi^T, Blo^T (N x Kp, K-major: B transposed) to a workspace;
+//   * split_kernel (one launch) writes Ahi, Alo (M x Kp, K-major like A) and
+//     Bhi^T, Blo^T (N x Kp, K-major: B transposed) to a workspace;
 //   * warp 0, one thread: TMA loads of the four K-major 128-byte-swizzled tiles
 //     of a k-block into a STAGES-deep ring, signalled through mbarriers;
 //   * warp 1, one thread: allocates tensor memory and issues
@@ -419,77 +419,108 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
     lo = __uint_as_float(r);
 }
 
-// Ahi/Alo[i*Kp + k] for i < M, k < Kp (zeros for K <= k < Kp).  Each thread
-// writes 4 consecutive k of one row as one float4 of hi and one of lo; it reads
-// A with a float4 too when the row is 16-byte aligned (vec_in) and whole.
-__global__ void __launch_bounds__(256) split_a_kernel(const float* __restrict__ A, long long lda,
-                                                      int M, int K, int Kp, int vec_in,
-                                                      float* __restrict__ hi,
-                                                      float* __restrict__ lo) {
-    const int k = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
-    if (k >= Kp) return;
-    for (int i = blockIdx.y; i < M; i += gridDim.y) {
-        const float* arow = A + static_cast<long long>(i) * lda;
-        float x[4];
-        if (vec_in && k + 3 < K) {
-            const float4 t = __ldg(reinterpret_cast<const float4*>(arow + k));
-            x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
-        } else {
+// Ahi/Alo[i*Kp + k] for i < M, k < Kp (zeros for K <= k < Kp): chunk e of the
+// M x Kp/4 float4 chunks is row e / (Kp/4), k = 4 (e % (Kp/4)).  Each chunk is
+// read as one float4 when A's row is 16-byte aligned (vec_in) and whole.
+__device__ __forceinline__ void split_a_chunk(const float* __restrict__ A, long long lda, int K,
+                                              int Kp, int vec_in, long long e,
+                                              float* __restrict__ hi, float* __restrict__ lo) {
+    const int kp4 = Kp / 4;
+    const long long i = e / kp4;
+    const int k = 4 * static_cast<int>(e - i * kp4);
+    const float* arow = A + i * lda;
+    float x[4];
+    if (vec_in && k + 3 < K) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(arow + k));
+        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+    } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) x[u] = (k + u < K) ? __ldg(arow + k + u) : 0.0f;
-        }
-        float h[4], l[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) split_tf32(x[u], h[u], l[u]);
-        const long long o = static_cast<long long>(i) * Kp + k;
-        *reinterpret_cast<float4*>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<float4*>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
+        for (int u = 0; u < 4; ++u) x[u] = (k + u < K) ? __ldg(arow + k + u) : 0.0f;
     }
+    float h[4], l[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) split_tf32(x[u], h[u], l[u]);
+    const long long o = i * Kp + k;
+    *reinterpret_cast<float4*>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<float4*>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
 }
 
-// Bhi/Blo[n*Kp + k] = split(B[k*ldb + n]) for n < N, k < Kp, through a 64 x 64
-// shared tile: reads along n and writes along k, both as float4 (reads fall back
-// to scalars when B's rows are not 16-byte aligned).
-constexpr int kTT = 64;
-__global__ void __launch_bounds__(256) split_bt_kernel(const float* __restrict__ B, long long ldb,
-                                                       int K, int N, int Kp, int vec_in,
-                                                       float* __restrict__ hi,
-                                                       float* __restrict__ lo) {
-    __shared__ float th[kTT][kTT + 1];
-    __shared__ float tl[kTT][kTT + 1];
-    const int k0 = blockIdx.y * kTT, n0 = blockIdx.x * kTT;
-    const int c4 = (threadIdx.x & 15) * 4;   // 16 threads x 4 columns per row
-    const int r0 = threadIdx.x >> 4;         // 16 rows per pass
+// Bhi/Blo[n*Kp + k] = split(B[k*ldb + n]) for the tile of kTK k by kTN n at
+// (k0, n0), through shared memory (row stride kTN + 1: conflict-free transposed
+// reads): reads along n and writes along k, both as float4 (reads fall back to
+// scalars when B's rows are not 16-byte aligned).  16.6 KB of shared memory, so
+// the split kernel keeps full occupancy for the blocks that split A.
+constexpr int kTK = 32, kTN = 64;
+__device__ __forceinline__ void split_bt_tile(const float* __restrict__ B, long long ldb, int K,
+                                              int N, int Kp, int vec_in, int k0, int n0,
+                                              float (&th)[kTK][kTN + 1],
+                                              float (&tl)[kTK][kTN + 1],
+                                              float* __restrict__ hi, float* __restrict__ lo) {
+    {
+        const int c4 = (threadIdx.x & 15) * 4;   // n within the tile: 16 threads x 4
+        const int r0 = threadIdx.x >> 4;         // k within the tile: 16 rows per pass
 #pragma unroll
-    for (int pass = 0; pass < kTT / 16; ++pass) {
-        const int r = r0 + 16 * pass;        // k within the tile
-        const int k = k0 + r, n = n0 + c4;
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (k < K) {
-            const float* brow = B + static_cast<long long>(k) * ldb;
-            if (vec_in && n + 3 < N) {
-                const float4 t = __ldg(reinterpret_cast<const float4*>(brow + n));
-                x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
-            } else {
+        for (int pass = 0; pass < kTK / 16; ++pass) {
+            const int r = r0 + 16 * pass;
+            const int k = k0 + r, n = n0 + c4;
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            if (k < K) {
+                const float* brow = B + static_cast<long long>(k) * ldb;
+                if (vec_in && n + 3 < N) {
+                    const float4 t = __ldg(reinterpret_cast<const float4*>(brow + n));
+                    x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+                } else {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) x[u] = (n + u < N) ? __ldg(brow + n + u) : 0.0f;
+                    for (int u = 0; u < 4; ++u) x[u] = (n + u < N) ? __ldg(brow + n + u) : 0.0f;
+                }
             }
-        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) split_tf32(x[u], th[r][c4 + u], tl[r][c4 + u]);
+            for (int u = 0; u < 4; ++u) split_tf32(x[u], th[r][c4 + u], tl[r][c4 + u]);
+        }
     }
     __syncthreads();
+    {
+        const int c4 = (threadIdx.x & 7) * 4;    // k within the tile: 8 threads x 4
+        const int r0 = threadIdx.x >> 3;         // n within the tile: 32 rows per pass
 #pragma unroll
-    for (int pass = 0; pass < kTT / 16; ++pass) {
-        const int nr = r0 + 16 * pass;       // n within the tile
-        const int n = n0 + nr, k = k0 + c4;
-        if (n < N && k < Kp) {
-            const long long o = static_cast<long long>(n) * Kp + k;
-            *reinterpret_cast<float4*>(hi + o) =
-                make_float4(th[c4][nr], th[c4 + 1][nr], th[c4 + 2][nr], th[c4 + 3][nr]);
-            *reinterpret_cast<float4*>(lo + o) =
-                make_float4(tl[c4][nr], tl[c4 + 1][nr], tl[c4 + 2][nr], tl[c4 + 3][nr]);
+        for (int pass = 0; pass < kTN / 32; ++pass) {
+            const int nr = r0 + 32 * pass;
+            const int n = n0 + nr, k = k0 + c4;
+            if (n < N && k < Kp) {
+                const long long o = static_cast<long long>(n) * Kp + k;
+                *reinterpret_cast<float4*>(hi + o) =
+                    make_float4(th[c4][nr], th[c4 + 1][nr], th[c4 + 2][nr], th[c4 + 3][nr]);
+                *reinterpret_cast<float4*>(lo + o) =
+                    make_float4(tl[c4][nr], tl[c4 + 1][nr], tl[c4 + 2][nr], tl[c4 + 3][nr]);
+            }
         }
+    }
+    __syncthreads();
+}
+
+// Both splits in one launch: blocks [0, a_blocks) stride over A's float4 chunks,
+// the others take the tiles of B in turn.
+__global__ void __launch_bounds__(256) split_kernel(
+    const float* __restrict__ A, long long lda, int M, const float* __restrict__ B,
+    long long ldb, int N, int K, int Kp, int a_vec, int b_vec, int a_blocks,
+    float* __restrict__ ahi, float* __restrict__ alo, float* __restrict__ bhi,
+    float* __restrict__ blo) {
+    if (static_cast<int>(blockIdx.x) < a_blocks) {
+        const long long chunks = static_cast<long long>(M) * (Kp / 4);
+        for (long long e = blockIdx.x * 256LL + threadIdx.x; e < chunks;
+             e += static_cast<long long>(a_blocks) * 256)
+            split_a_chunk(A, lda, K, Kp, a_vec, e, ahi, alo);
+        return;
+    }
+    __shared__ float th[kTK][kTN + 1];
+    __shared__ float tl[kTK][kTN + 1];
+    const int tiles_n = (N + kTN - 1) / kTN;
+    const long long tiles = static_cast<long long>(tiles_n) * ((Kp + kTK - 1) / kTK);
+    const int b_blocks = static_cast<int>(gridDim.x) - a_blocks;
+    for (long long t = static_cast<int>(blockIdx.x) - a_blocks; t < tiles; t += b_blocks) {
+        const int tk = static_cast<int>(t / tiles_n);
+        const int tn = static_cast<int>(t - static_cast<long long>(tk) * tiles_n);
+        split_bt_tile(B, ldb, K, N, Kp, b_vec, tk * kTK, tn * kTN, th, tl, bhi, blo);
     }
 }
 
@@ -651,17 +682,20 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
     }
     const int Kp = (K + 3) / 4 * 4;
     const WsLayout L = ws_layout(ws, M, N, Kp);
-    (void)sms;
-    if ((Kp + kTT - 1) / kTT > 65535) {
-        set_last_error_message("tf32x3: K too large for the split kernels' grid");
-        return SGEMM_ERR_UNSUPPORTED;
-    }
     const int a_vec = ((reinterpret_cast<uintptr_t>(A) & 15) == 0 && lda % 4 == 0) ? 1 : 0;
     const int b_vec = ((reinterpret_cast<uintptr_t>(B) & 15) == 0 && ldb % 4 == 0) ? 1 : 0;
-    const dim3 ga((Kp / 4 + 255) / 256, std::min(M, 65535));
-    split_a_kernel<<<ga, 256, 0, stream>>>(A, lda, M, K, Kp, a_vec, L.ahi, L.alo);
-    const dim3 gb((N + kTT - 1) / kTT, (Kp + kTT - 1) / kTT);
-    split_bt_kernel<<<gb, 256, 0, stream>>>(B, ldb, K, N, Kp, b_vec, L.bhi, L.blo);
+    // One float4 chunk of A per thread and one 32 x 64 tile of B per block (the
+    // kernel strides if the grid would exceed the launch limit): plenty of loads
+    // in flight for large operands, and a single launch for small ones.
+    const long long a_chunks = static_cast<long long>(M) * (Kp / 4);
+    const long long b_tiles = static_cast<long long>((N + kTN - 1) / kTN) * ((Kp + kTK - 1) / kTK);
+    const long long cap = 1LL << 30;
+    const long long a_blocks = std::min((a_chunks + 255) / 256, cap);
+    const long long b_blocks = std::min(b_tiles, cap);
+    (void)sms;
+    split_kernel<<<static_cast<unsigned>(a_blocks + b_blocks), 256, 0, stream>>>(
+        A, lda, M, B, ldb, N, K, Kp, a_vec, b_vec, static_cast<int>(a_blocks), L.ahi, L.alo,
+        L.bhi, L.blo);
     if (cudaGetLastError() != cudaSuccess) {
         set_last_error_message("tf32x3: split kernels failed to launch");
         return SGEMM_ERR_LAUNCH;
