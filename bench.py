@@ -42,7 +42,7 @@ def describe(w) -> str:
 
 # Files whose text is the code of the FFMA kernels (the tile-table entry name
 # encodes the template parameters).
-KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_internal.h", "sgemm_epilogue.cuh"]
+KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_args.h", "sgemm_epilogue.cuh"]
 
 
 def kernel_sources_hash() -> str:

@@ -9,7 +9,7 @@
 // already checked the row.
 #pragma once
 
-#include "sgemm_internal.h"
+#include "sgemm_args.h"
 
 namespace sgemm {
 

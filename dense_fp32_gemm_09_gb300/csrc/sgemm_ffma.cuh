@@ -37,7 +37,7 @@
 #include <stdint.h>
 
 #include "sgemm_epilogue.cuh"
-#include "sgemm_internal.h"
+#include "sgemm_args.h"
 #include "sgemm_sched.cuh"
 
 namespace sgemm {

@@ -11,7 +11,7 @@
 
 #include <stddef.h>
 
-#include "sgemm_internal.h"
+#include "sgemm_args.h"
 
 namespace sgemm {
 
