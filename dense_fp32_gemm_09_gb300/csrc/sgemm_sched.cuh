@@ -117,7 +117,10 @@ inline SchedSizes plan_schedule(GemmArgs& a, int bm, int bn, int bk, int sms, in
     a.tiles_m = (a.M + bm - 1) / bm;
     a.tiles_n = (a.N + bn - 1) / bn;
     a.KT = (a.K + bk - 1) / bk;
-    a.group_m = a.tiles_m < 8 ? a.tiles_m : 8;
+    // 16 tile rows per raster group: a wave of ~152 tiles then spans about 16 rows
+    // x 9.5 columns rather than 8 rows x all columns, so each wave reads A rows
+    // and B columns in a ratio near the optimum (fewer repeated B reads from DRAM).
+    a.group_m = a.tiles_m < 16 ? a.tiles_m : 16;
     const long long T = static_cast<long long>(a.tiles_m) * a.tiles_n;
     long long Gmax = static_cast<long long>(sms) * occ;
     if (Gmax > kMaxSkTiles) Gmax = kMaxSkTiles;
