@@ -58,3 +58,13 @@ def test_rejects_bad_arguments(lib):
     assert lib.sgemm_schedule_check(0, 4, 4, 0, 152, 2, 0, None) == -1
     assert lib.sgemm_schedule_check(4, 4, 4, 0, 0, 2, 0, None) == -1
     assert lib.sgemm_schedule_check(4, 4, 4, 999, 152, 2, 0, None) == -1
+
+
+@pytest.mark.parametrize("M,N,K", [(67000, 64, 32768), (50000, 45000, 8)])
+def test_schedule_of_operands_past_2_31_elements(lib, M, N, K):
+    """The shapes of the GPU tests whose A or C hold more than 2**31 elements."""
+    for kid in range(lib.sgemm_num_kernels()):
+        for sms, occ in [(152, 1), (152, 4)]:
+            cfg = _cfg()
+            rc = lib.sgemm_schedule_check(M, N, K, kid, sms, occ, 0, ctypes.byref(cfg))
+            assert rc == 0, (kid, sms, occ, lib.sgemm_last_error())
