@@ -363,33 +363,33 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
                     else if (m0 + tr < a.M)
                         store_c4(a, a.C + static_cast<long long>(m0 + tr) * a.ldc, n0 + tc, v);
                 }
-                continue;
-            }
-            // Stores go through a 32 x 32 staging block per warp (16-byte chunks
-            // XOR-swizzled by row, so both the row-wise writes and the column-wise
-            // reads are conflict-free): each store instruction then covers four
-            // whole 128-byte row segments instead of 32 scattered 16-byte pieces.
+            } else {
+                // Stores go through a 32 x 32 staging block per warp (16-byte chunks
+                // XOR-swizzled by row, so both the row-wise writes and the column-wise
+                // reads are conflict-free): each store instruction then covers four
+                // whole 128-byte row segments instead of 32 scattered 16-byte pieces.
 #pragma unroll
-            for (int j = 0; j < EC / 32; ++j) {
-                __syncwarp();
+                for (int j = 0; j < EC / 32; ++j) {
+                    __syncwarp();
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) * 4)) =
-                        make_float4(sum[32 * j + 4 * u], sum[32 * j + 4 * u + 1],
-                                    sum[32 * j + 4 * u + 2], sum[32 * j + 4 * u + 3]);
-                __syncwarp();
-                const int c4 = lane & 7;
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<float4*>(stg + lane * 32 + ((u ^ (lane & 7)) * 4)) =
+                            make_float4(sum[32 * j + 4 * u], sum[32 * j + 4 * u + 1],
+                                        sum[32 * j + 4 * u + 2], sum[32 * j + 4 * u + 3]);
+                    __syncwarp();
+                    const int c4 = lane & 7;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = 4 * i + (lane >> 3);            // row in the block
-                    const float4 v =
-                        *reinterpret_cast<const float4*>(stg + rr * 32 + ((c4 ^ (rr & 7)) * 4));
-                    const int tr = 32 * q + rr;                    // row of the tile
-                    const int tc = col0 + 32 * j + 4 * c4;         // column of the tile
-                    if (partial) {
-                        __stcg(reinterpret_cast<float4*>(P + tr * BN + tc), v);
-                    } else if (m0 + tr < a.M) {
-                        store_c4(a, a.C + static_cast<long long>(m0 + tr) * a.ldc, n0 + tc, v);
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = 4 * i + (lane >> 3);            // row in the block
+                        const float4 v =
+                            *reinterpret_cast<const float4*>(stg + rr * 32 + ((c4 ^ (rr & 7)) * 4));
+                        const int tr = 32 * q + rr;                    // row of the tile
+                        const int tc = col0 + 32 * j + 4 * c4;         // column of the tile
+                        if (partial) {
+                            __stcg(reinterpret_cast<float4*>(P + tr * BN + tc), v);
+                        } else if (m0 + tr < a.M) {
+                            store_c4(a, a.C + static_cast<long long>(m0 + tr) * a.ldc, n0 + tc, v);
+                        }
                     }
                 }
             }
