@@ -91,8 +91,10 @@ typedef struct {
  * a larger one is needed, freed by sgemm_shutdown).  Large problems (M*N*K >=
  * 2^31) whose A or B rows are not 16-byte aligned are first copied row by row
  * into aligned buffers in that workspace (one more launch per copied operand),
- * so they run on the 16-byte / TMA kernels; the results are the same as without
- * the copy (the copy moves values, not sums).  The first call that needs
+ * so they run on the 16-byte / TMA kernels (the copy moves values, not sums: the
+ * results are those of the aligned kernels on aligned operands; they can differ
+ * from the 4-byte-load kernels' in rounding, as any two tilings can, and stay
+ * within the same bound).  The first call that needs
  * a workspace must not be made while the stream is being captured into a CUDA
  * graph. */
 SGEMM_API int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
@@ -185,9 +187,13 @@ SGEMM_API int sgemm_run_op(int transa, int transb, int M, int N, int K, float al
  * and copies C back to hC.  The work is ordered after everything already queued
  * on `stream`, and `stream` waits for all of it, so it behaves as if issued on
  * `stream`; inside, it runs on three library-owned streams of the current device
- * (created on first use, destroyed by sgemm_shutdown): B is copied first, then A
- * and C go in row panels of C, so that one panel's copies overlap another
- * panel's product.  The call returns when the work is queued; synchronise
+ * (created on first use, destroyed by sgemm_shutdown) so that copies overlap the
+ * product: C is computed in row panels; the first panel's product is summed over
+ * k-chunks (beta = 1 after the first) as its chunk of A and B arrives, the other
+ * panels start once their rows of A are in, and each finished panel is copied
+ * back while the next one is computed.  Rounding can differ from sgemm_run's by
+ * that chunking; the error bound is the same.  The call returns when the work is
+ * queued; synchronise
  * `stream` before reading hC.  Calls from several host threads are serialised
  * while they queue.  Errors: as sgemm_run, plus SGEMM_ERR_INVALID_ARG for a null
  * device buffer with a non-empty extent and SGEMM_ERR_LAUNCH for a failed copy;
@@ -205,8 +211,10 @@ SGEMM_API int sgemm_run_host(int M, int N, int K, const float* hA, int lda, cons
  * NaN inputs are not supported (the split turns Inf into NaN).  The split
  * operands go to a workspace of sgemm_tf32x3_workspace_size() bytes: the caller's
  * `ws` (16-byte aligned, ws_bytes large enough) or, when ws is NULL, the library's
- * per-stream workspace (allocated on first use).  Launches three kernels (two
- * splits, one GEMM).  Any alignment of A, B, C and any leading dimensions.
+ * per-stream workspace (allocated on first use).  The workspace also holds the
+ * partial tiles when the schedule splits tiles between CTAs.  Launches the
+ * operand split, the GEMM and, for split tiles, a deterministic reduction.  Any
+ * alignment of A, B, C and any leading dimensions.
  * Bounded device-side waits that give up set a flag read by sgemm_device_status(). */
 SGEMM_API int sgemm_tf32x3_run(int M, int N, int K, const float* A, int lda, const float* B,
                                int ldb, float* C, int ldc, sgemm_stream_t stream);
