@@ -41,6 +41,7 @@
 #include "sgemm_epilogue.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_sched.cuh"
+#include "sgemm_tma_host.h"
 
 namespace sgemm {
 namespace tc {
@@ -539,33 +540,10 @@ struct Variant {
         (BN == 128 ? static_cast<size_t>(4) * kStageFloats * 4 : 0);   // + epilogue staging
 };
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// rows x K fp32 matrix with row pitch Kp floats; box = 32 (K) x box_rows.
+// rows x K fp32 matrix with row pitch Kp floats; boxes of 32 (K) x box_rows with
+// the 128-byte swizzle the UMMA descriptors expect.
 bool encode_kmajor(CUtensorMap* tm, const float* base, int rows, int K, int Kp, int box_rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(Kp) * 4};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-    cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_fp32_2d(tm, base, rows, K, Kp, BK, box_rows, /*swizzle128=*/true);
 }
 
 size_t region_floats(long long rows, int Kp) {
