@@ -21,8 +21,19 @@ int run_wait_selftest(int limit_ms);
 cudaError_t launch_sk_reduce(const GemmArgs& a, int bm, int bn, int sms, cudaStream_t stream);
 int reduce_chunks(int bm, int bn, int sk_tiles, int sms);
 
-// Sets the text sgemm_last_error() returns on this thread.
+// Sets the text sgemm_last_error() returns on this thread: a plain message, or
+// "<what>: <CUDA error name> (<description>)".
 void set_last_error_message(const char* msg);
+void set_cuda_error(const char* what, cudaError_t e);
+
+// Argument checks of the public entry points (sizes, leading dimensions of the
+// stored operands, null pointers, C overlapping A or B); op = 1 means the operand
+// is stored transposed.  SGEMM_OK or SGEMM_ERR_INVALID_ARG with a message.
+int check_operands(int transa, int transb, int M, int N, int K, const float* A, int lda,
+                   const float* B, int ldb, const float* C, int ldc);
+
+// Destroys the host-buffer entry point's streams and events (sgemm_shutdown).
+void shutdown_host_pipes();
 
 // 3xTF32 tensor-core path (sgemm_tf32x3.cu).
 size_t tf32x3_workspace_bytes(int M, int N, int K);
