@@ -180,7 +180,7 @@ struct Acc<TM, TN, true, BOUTER> {
 // The kernel
 // ----------------------------------------------------------------------------
 template <int BM_, int BN_, int BK_, int TM_, int TN_, int LR_, int WARPS_M_, int WARPS_N_,
-          int STAGES_, int VEC_, int AK_, bool FMA2_, int MINB_>
+          int STAGES_, int VEC_, int AK_, bool FMA2_, int MINB_, bool PIPE_ = false>
 struct FfmaCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, TM = TM_, TN = TN_;
     static constexpr int LR = LR_, LC = 32 / LR_;
@@ -190,6 +190,9 @@ struct FfmaCfg {
     static constexpr int STAGES = STAGES_, VEC = VEC_, AK = AK_;
     static constexpr bool FMA2 = FMA2_;
     static constexpr int MINB = MINB_;
+    // PIPE: load the next k's fragments before the current k's FMAs (register
+    // double buffering of A and B fragments inside a slice).
+    static constexpr bool PIPE = PIPE_;
     // A slice: [BM][BK + PADA] (row stride odd in 16-byte units); B slice: [BK][BN].
     static constexpr int PADA = ((BK / 4) % 2 == 0) ? 4 : 0;
     static constexpr int LDAS = BK + PADA;
@@ -271,38 +274,74 @@ __device__ __forceinline__ void load_slice(const GemmArgs& a, float* sA, float* 
 }
 
 // One BK-deep slice of rank-1 updates from shared memory into the registers.
+// Fragments of one slice: A as AK consecutive k of each of the thread's TM rows
+// (one 16- or 8-byte load per row), B as TN values of one k.
+template <class Cfg>
+__device__ __forceinline__ void load_a_frag(const float* sA, int a_row0, int kq,
+                                            float (&av)[Cfg::TM][Cfg::AK]) {
+    constexpr int TM = Cfg::TM, AK = Cfg::AK, LR = Cfg::LR, LDAS = Cfg::LDAS;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const float* p = sA + (a_row0 + i * LR) * LDAS + kq;
+        if constexpr (AK == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(p);
+            av[i][0] = t.x; av[i][1] = t.y; av[i][2] = t.z; av[i][3] = t.w;
+        } else if constexpr (AK == 2) {
+            const float2 t = *reinterpret_cast<const float2*>(p);
+            av[i][0] = t.x; av[i][1] = t.y;
+        } else {
+            av[i][0] = *p;
+        }
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void load_b_frag(const float* sB, int b_col0, int k,
+                                            float4 (&b)[Cfg::TN / 4]) {
+#pragma unroll
+    for (int j4 = 0; j4 < Cfg::TN / 4; ++j4)
+        b[j4] = *reinterpret_cast<const float4*>(sB + k * Cfg::LDBS + b_col0 + j4 * Cfg::LC * 4);
+}
+
 template <class Cfg, class AccT>
 __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, int a_row0,
                                               int b_col0, AccT& acc) {
     constexpr int BK = Cfg::BK, TM = Cfg::TM, TN = Cfg::TN, AK = Cfg::AK;
-    constexpr int LR = Cfg::LR, LC = Cfg::LC, LDAS = Cfg::LDAS, LDBS = Cfg::LDBS;
+    if constexpr (Cfg::PIPE) {
+        // Two fragment sets: the loads for the next step are issued before the
+        // current step's FMAs, so shared-memory latency hides behind them.
+        float av[2][TM][AK];
+        float4 b[2][TN / 4];
+        load_a_frag<Cfg>(sA, a_row0, 0, av[0]);
+        load_b_frag<Cfg>(sB, b_col0, 0, b[0]);
 #pragma unroll
-    for (int kq = 0; kq < BK; kq += AK) {
-        float av[TM][AK];
+        for (int kq = 0; kq < BK; kq += AK) {
+            const int ab = (kq / AK) & 1;
+            if (kq + AK < BK) load_a_frag<Cfg>(sA, a_row0, kq + AK, av[ab ^ 1]);
 #pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const float* p = sA + (a_row0 + i * LR) * LDAS + kq;
-            if constexpr (AK == 4) {
-                const float4 t = *reinterpret_cast<const float4*>(p);
-                av[i][0] = t.x; av[i][1] = t.y; av[i][2] = t.z; av[i][3] = t.w;
-            } else if constexpr (AK == 2) {
-                const float2 t = *reinterpret_cast<const float2*>(p);
-                av[i][0] = t.x; av[i][1] = t.y;
-            } else {
-                av[i][0] = *p;
+            for (int kk = 0; kk < AK; ++kk) {
+                const int k = kq + kk, bb = k & 1;
+                if (k + 1 < BK) load_b_frag<Cfg>(sB, b_col0, k + 1, b[bb ^ 1]);
+                float ak[TM];
+#pragma unroll
+                for (int i = 0; i < TM; ++i) ak[i] = av[ab][i][kk];
+                acc.rank1(ak, b[bb]);
             }
         }
+    } else {
 #pragma unroll
-        for (int kk = 0; kk < AK; ++kk) {
-            float4 b[TN / 4];
+        for (int kq = 0; kq < BK; kq += AK) {
+            float av[TM][AK];
+            load_a_frag<Cfg>(sA, a_row0, kq, av);
 #pragma unroll
-            for (int j4 = 0; j4 < TN / 4; ++j4)
-                b[j4] = *reinterpret_cast<const float4*>(sB + (kq + kk) * LDBS + b_col0 +
-                                                         j4 * LC * 4);
-            float ak[TM];
+            for (int kk = 0; kk < AK; ++kk) {
+                float4 b[TN / 4];
+                load_b_frag<Cfg>(sB, b_col0, kq + kk, b);
+                float ak[TM];
 #pragma unroll
-            for (int i = 0; i < TM; ++i) ak[i] = av[i][kk];
-            acc.rank1(ak, b);
+                for (int i = 0; i < TM; ++i) ak[i] = av[i][kk];
+                acc.rank1(ak, b);
+            }
         }
     }
 }
