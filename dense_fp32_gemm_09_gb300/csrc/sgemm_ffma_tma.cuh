@@ -46,38 +46,49 @@ struct TmaLayout {
     static_assert(Cfg::BN <= 256 && Cfg::BK <= 256 && Cfg::BM <= 256, "TMA box limits");
 };
 
+// A fragments of AK consecutive k (one 16- or 8-byte load per row) from the
+// swizzled A slice; B values of one k.
+template <class Cfg>
+__device__ __forceinline__ void load_a_frag_tma(const float* sA, int a_row0, int lr4, int kq,
+                                                float (&av)[Cfg::TM][Cfg::AK]) {
+    constexpr int BM = Cfg::BM, TM = Cfg::TM, LR = Cfg::LR, AK = Cfg::AK;
+    const int h = kq / 32, c = (kq % 32) / 4, sub = kq % 4;
+    const int oe = ((c * 4) ^ lr4) + sub;   // rows with r & 7 == lr
+    const int oo = oe ^ 16;                 // rows with r & 7 == lr + 4
+    const float* ah = sA + a_row0 * 32 + h * BM * 32;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const float* pa = ah + i * LR * 32 + ((i & 1) ? oo : oe);
+        if constexpr (AK == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(pa);
+            av[i][0] = t.x; av[i][1] = t.y; av[i][2] = t.z; av[i][3] = t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2*>(pa);
+            av[i][0] = t.x; av[i][1] = t.y;
+        }
+    }
+}
+
+template <class Cfg>
+__device__ __forceinline__ void load_b_frag_tma(const float* sB, int b_col0, int k,
+                                                float4 (&b)[Cfg::TN / 4]) {
+#pragma unroll
+    for (int j4 = 0; j4 < Cfg::TN / 4; ++j4)
+        b[j4] = *reinterpret_cast<const float4*>(sB + k * Cfg::BN + b_col0 + j4 * Cfg::LC * 4);
+}
+
 template <class Cfg, class AccT>
 __device__ __forceinline__ void compute_slice_tma(const float* sA, const float* sB, int a_row0,
                                                   int lr4, int b_col0, AccT& acc) {
-    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, TM = Cfg::TM, TN = Cfg::TN;
-    constexpr int LR = Cfg::LR, LC = Cfg::LC;
-    constexpr int AK = Cfg::AK;
-    const float* a_row = sA + a_row0 * 32;
+    constexpr int BK = Cfg::BK, TM = Cfg::TM, TN = Cfg::TN, AK = Cfg::AK;
 #pragma unroll
     for (int kq = 0; kq < BK; kq += AK) {
-        const int h = kq / 32, c = (kq % 32) / 4, sub = kq % 4;
-        const int oe = ((c * 4) ^ lr4) + sub;   // rows with r & 7 == lr
-        const int oo = oe ^ 16;                 // rows with r & 7 == lr + 4
-        const float* ah = a_row + h * BM * 32;
         float av[TM][AK];
-#pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const float* pa = ah + i * LR * 32 + ((i & 1) ? oo : oe);
-            if constexpr (AK == 4) {
-                const float4 t = *reinterpret_cast<const float4*>(pa);
-                av[i][0] = t.x; av[i][1] = t.y; av[i][2] = t.z; av[i][3] = t.w;
-            } else {
-                const float2 t = *reinterpret_cast<const float2*>(pa);
-                av[i][0] = t.x; av[i][1] = t.y;
-            }
-        }
+        load_a_frag_tma<Cfg>(sA, a_row0, lr4, kq, av);
 #pragma unroll
         for (int kk = 0; kk < AK; ++kk) {
             float4 b[TN / 4];
-#pragma unroll
-            for (int j4 = 0; j4 < TN / 4; ++j4)
-                b[j4] = *reinterpret_cast<const float4*>(sB + (kq + kk) * BN + b_col0 +
-                                                         j4 * LC * 4);
+            load_b_frag_tma<Cfg>(sB, b_col0, kq + kk, b);
             float ak[TM];
 #pragma unroll
             for (int i = 0; i < TM; ++i) ak[i] = av[i][kk];
