@@ -1,0 +1,97 @@
+"""Seeded random cases across the whole entry-point surface, each checked element
+by element against the fp64 oracle (oracle_gemm_f64_op): random M, N, K, leading
+dimension padding, 4-byte misalignment of the bases, alpha/beta (including 0 and
+1) and transpose flags; C lives inside a canary-filled buffer.  The 3xTF32 path
+gets its own random cases at its own tolerance."""
+import numpy as np
+import pytest
+
+from dense_fp32_gemm_09_gb300 import check, load, sgemm_run_op
+
+pytestmark = pytest.mark.gpu
+
+CANARY = -7.25
+
+
+def case(rng):
+    M, N, K = (int(x) for x in rng.integers(1, 700, size=3))
+    if rng.random() < 0.1:
+        K = int(rng.integers(1, 5))
+    ta, tb = int(rng.integers(0, 2)), int(rng.integers(0, 2))
+    alpha = float(rng.choice([1.0, 0.0, -1.5, 0.25]))
+    beta = float(rng.choice([0.0, 1.0, -0.5, 2.0]))
+    pads = [int(x) for x in rng.integers(0, 6, size=3)]
+    offs = [int(x) for x in rng.integers(0, 2, size=3)]
+    return M, N, K, ta, tb, alpha, beta, pads, offs
+
+
+def place(torch, X, pad, off, fill):
+    rows, cols = X.shape
+    ld = cols + pad
+    flat = torch.full((off + rows * ld + 4,), fill, dtype=torch.float32, device="cuda")
+    view = flat[off:off + rows * ld].view(rows, ld)[:, :cols]
+    view.copy_(X)
+    return flat, view, ld
+
+
+@pytest.mark.parametrize("seed", range(120))
+def test_random_ffma_cases(cuda, oracle_mod, seed):
+    torch = cuda
+    rng = np.random.default_rng(1000 + seed)
+    M, N, K, ta, tb, alpha, beta, pads, offs = case(rng)
+    g = torch.Generator().manual_seed(seed)
+    A = torch.rand(M, K, generator=g) * 2 - 1                  # logical operands
+    B = torch.rand(K, N, generator=g) * 2 - 1
+    C0 = torch.rand(M, N, generator=g) * 2 - 1
+    _, dA, lda = place(torch, A.t().contiguous() if ta else A, pads[0], offs[0], float("nan"))
+    _, dB, ldb = place(torch, B.t().contiguous() if tb else B, pads[1], offs[1], float("nan"))
+    cbuf, dC, ldc = place(torch, C0, pads[2], offs[2], CANARY)
+    st = sgemm_run_op(ta, tb, M, N, K, alpha, dA.data_ptr(), lda, dB.data_ptr(), ldb, beta,
+                      dC.data_ptr(), ldc)
+    assert st == 0, (M, N, K, ta, tb, load().sgemm_last_error())
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm_f64_op(ta, tb, dA.cpu().numpy(), dB.cpu().numpy(), alpha, beta,
+                                 C0.numpy())
+    err = np.max(np.abs(dC.cpu().numpy().astype(np.float64) - ref))
+    tol = 1e-6 * (abs(alpha) * K + abs(beta)) + 1e-30
+    assert err <= tol, ((M, N, K, ta, tb, alpha, beta, pads, offs), err, tol)
+    # nothing outside C was written
+    flat = cbuf.cpu().numpy()
+    mask = np.ones(flat.size, dtype=bool)
+    base = offs[2]
+    for r in range(M):
+        mask[base + r * ldc: base + r * ldc + N] = False
+    assert np.all(flat[mask] == CANARY)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_tf32x3_cases(cuda, oracle_mod, seed):
+    torch = cuda
+    lib = load()
+    rng = np.random.default_rng(2000 + seed)
+    M, N, K = (int(x) for x in rng.integers(1, 900, size=3))
+    alpha = float(rng.choice([1.0, -2.0, 0.5]))
+    beta = float(rng.choice([0.0, 1.0, -0.75]))
+    pads = [int(x) for x in rng.integers(0, 6, size=3)]
+    offs = [int(x) for x in rng.integers(0, 2, size=3)]
+    g = torch.Generator().manual_seed(100 + seed)
+    A = torch.rand(M, K, generator=g) * 2 - 1
+    B = torch.rand(K, N, generator=g) * 2 - 1
+    C0 = torch.rand(M, N, generator=g) * 2 - 1
+    _, dA, lda = place(torch, A, pads[0], offs[0], float("nan"))
+    _, dB, ldb = place(torch, B, pads[1], offs[1], float("nan"))
+    cbuf, dC, ldc = place(torch, C0, pads[2], offs[2], CANARY)
+    check(lib.sgemm_tf32x3_run_ex(M, N, K, alpha, dA.data_ptr(), lda, dB.data_ptr(), ldb, beta,
+                                  dC.data_ptr(), ldc, None, 0,
+                                  torch.cuda.current_stream().cuda_stream), "tf32x3")
+    torch.cuda.synchronize()
+    check(lib.sgemm_device_status(), "device status")
+    ref = oracle_mod.gemm_f64_ex(alpha, A.numpy(), B.numpy(), beta, C0.numpy())
+    err = np.max(np.abs(dC.cpu().numpy().astype(np.float64) - ref))
+    tol = 1e-5 * (abs(alpha) * K + abs(beta)) + 1e-30
+    assert err <= tol, ((M, N, K, alpha, beta, pads, offs), err, tol)
+    flat = cbuf.cpu().numpy()
+    mask = np.ones(flat.size, dtype=bool)
+    for r in range(M):
+        mask[offs[2] + r * ldc: offs[2] + r * ldc + N] = False
+    assert np.all(flat[mask] == CANARY)
