@@ -73,7 +73,7 @@ def test_p1_printed_output_fp32_fma(oracle_mod):
     assert printed == rows["C_row0_printed"]
 
 
-def test_p1_fp32_within_north_star_tolerance_of_f64(oracle_mod):
+def test_p1_fp32_close_to_f64(oracle_mod):
     A, B = p1_inputs()
     c32 = oracle_mod.gemm_f32_fma_seq(A, B).astype(np.float64)
     c64 = oracle_mod.gemm_f64(A, B)
