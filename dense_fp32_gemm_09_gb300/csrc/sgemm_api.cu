@@ -357,9 +357,8 @@ int launch(const Plan& p, cudaStream_t stream) {
     if (e.tma) {
         // A: 32 (k) x BM boxes, 128-byte swizzle; B: BN (n) x BK boxes, no swizzle.
         tp.g = p.args;
-        if (!encode_fp32_2d(&tp.ta, p.args.A, p.args.M, p.args.K, p.args.lda, 32, e.bm, true) ||
-            !encode_fp32_2d(&tp.tb, p.args.B, p.args.K, p.args.N, p.args.ldb, e.bn, e.bk,
-                            false)) {
+        if (!encode_fp32_2d(&tp.ta, p.args.A, p.args.M, p.args.K, p.args.lda, 32, e.bm, 128) ||
+            !encode_fp32_2d(&tp.tb, p.args.B, p.args.K, p.args.N, p.args.ldb, e.bn, e.bk, 0)) {
             std::snprintf(t_last_error, sizeof(t_last_error),
                           "%s: cuTensorMapEncodeTiled failed", e.name);
             return SGEMM_ERR_LAUNCH;

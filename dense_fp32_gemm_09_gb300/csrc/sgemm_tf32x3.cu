@@ -54,8 +54,8 @@ using async::su32;
 using async::tma_load_2d;
 
 constexpr int BM = 128;
-constexpr int BK = 32;        // fp32 per k-block row: one 128-byte swizzle row
 constexpr int UMMA_K = 8;     // K of one tcgen05.mma .kind::tf32
+constexpr int KCHUNK = 128;   // K accumulated per TMEM chunk (see the kernel)
 // warp 0: TMA, warp 1: MMA, then 4 epilogue warps per 128 accumulator columns
 __host__ __device__ constexpr int tf32x3_threads(int bn) { return 64 + 32 * 4 * (bn / 128); }
 
@@ -64,7 +64,7 @@ inline size_t align_up_floats(size_t n) { return (n + 63) / 64 * 64; }
 
 struct Params {
     CUtensorMap tm_ahi, tm_alo, tm_bhi, tm_blo;
-    // C, its epilogue, the persistent / stream-K schedule (k-blocks of BK), the
+    // C, its epilogue, the persistent / stream-K schedule (k-blocks of BKT), the
     // partial-tile workspace and the device status word; A and B are unused.
     GemmArgs s;
 };
@@ -112,15 +112,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA with
-// 128-byte swizzling: rows of 128 bytes, the swizzle pattern repeating every 8
-// rows (1024 bytes = the stride between 8-row groups), one swizzle atom along K.
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+// the swizzle matching its row width: BKT fp32 of K per row (32 -> 128-byte rows,
+// 128-byte swizzle; 16 -> 64-byte rows, 64-byte swizzle), the pattern repeating
+// every 8 rows (8 rows x row bytes = the stride between 8-row groups), one
+// swizzle atom along K.
+template <int BKT>
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t saddr) {
+    static_assert(BKT == 32 || BKT == 16, "k-block depth");
+    constexpr uint64_t kRowBytes = BKT * 4;
+    constexpr uint64_t kLayout = BKT == 32 ? 2 : 4;           // 128-byte / 64-byte swizzle
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);       // start address
     d |= static_cast<uint64_t>(0) << 16;                      // leading byte offset (unused)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;              // stride byte offset
+    d |= ((8 * kRowBytes) >> 4) << 32;                        // stride byte offset
     d |= static_cast<uint64_t>(1) << 46;                      // descriptor version
-    d |= static_cast<uint64_t>(2) << 61;                      // 128-byte swizzle
+    d |= kLayout << 61;                                       // swizzle mode
     return d;
 }
 
@@ -144,12 +150,13 @@ constexpr int kStageFloats = 32 * 32;   // epilogue staging block of one warp
 // MMAs of chunk c+1 overlap the epilogue's read of chunk c.  Chunk boundaries
 // are the multiples of KC_BLOCKS k-blocks (and the ends of a CTA's part of a
 // tile), so a tile computed whole is chunked the same way under any schedule.
-template <int BN, int STAGES, int KC_BLOCKS>
+template <int BN, int BKT, int STAGES>
 __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
     tf32x3_kernel(const __grid_constant__ Params p) {
     constexpr int EPI_WARPS = 4 * (BN / 128);
-    constexpr uint32_t A_BYTES = BM * BK * 4;
-    constexpr uint32_t B_BYTES = BN * BK * 4;
+    constexpr int KC_BLOCKS = KCHUNK / BKT;   // k-blocks per TMEM chunk
+    constexpr uint32_t A_BYTES = BM * BKT * 4;
+    constexpr uint32_t B_BYTES = BN * BKT * 4;
     constexpr uint32_t STAGE_BYTES = 2 * A_BYTES + 2 * B_BYTES;
     constexpr uint32_t TMEM_COLS = 2 * BN;   // two chunk accumulators
     constexpr bool STAGED = BN == 128;       // epilogue stores through shared memory
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
                 }
                 const uint32_t fb = su32(&full_bar[stage]);
                 const uint32_t base = smem0 + stage * STAGE_BYTES;
-                const int k0 = cur.kt * BK;
+                const int k0 = cur.kt * BKT;
                 mbar_expect_tx(fb, STAGE_BYTES);
                 tma_load_2d(base, &p.tm_ahi, k0, m0, fb);
                 tma_load_2d(base + A_BYTES, &p.tm_alo, k0, m0, fb);
@@ -272,12 +279,12 @@ __global__ void __launch_bounds__(tf32x3_threads(BN), 1)
                     tc_fence_after();
                     const uint32_t base = smem0 + stage * STAGE_BYTES;
 #pragma unroll
-                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                    for (int k = 0; k < BKT / UMMA_K; ++k) {
                         const uint32_t off = k * UMMA_K * 4;
-                        const uint64_t ahi = sw128_kmajor_desc(base + off);
-                        const uint64_t alo = sw128_kmajor_desc(base + A_BYTES + off);
-                        const uint64_t bhi = sw128_kmajor_desc(base + 2 * A_BYTES + off);
-                        const uint64_t blo = sw128_kmajor_desc(base + 2 * A_BYTES + B_BYTES + off);
+                        const uint64_t ahi = kmajor_desc<BKT>(base + off);
+                        const uint64_t alo = kmajor_desc<BKT>(base + A_BYTES + off);
+                        const uint64_t bhi = kmajor_desc<BKT>(base + 2 * A_BYTES + off);
+                        const uint64_t blo = kmajor_desc<BKT>(base + 2 * A_BYTES + B_BYTES + off);
                         umma_tf32(d_tmem, alo, bhi, idesc, (first && k == 0) ? 0u : 1u);
                         umma_tf32(d_tmem, ahi, blo, idesc, 1u);
                         umma_tf32(d_tmem, ahi, bhi, idesc, 1u);
@@ -528,22 +535,28 @@ __global__ void __launch_bounds__(256) split_kernel(
 // ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
-constexpr int kChunkBlocks = 4;   // 128 of K per TMEM chunk
-// Two output-tile widths: 128 columns with 3 pipeline stages, or 256 columns
-// with 2 (the shared-memory ring holds 192 KB either way).
+// Two output-tile widths, each with the k-block depth and ring depth that fill
+// about 192 KB of shared memory: 128 columns with 32-deep k-blocks and 3 stages
+// (64 KB each), 256 columns with 16-deep k-blocks and 4 stages (48 KB each).
+// The pipeline depth matters: 128 columns with 2 stages instead of 3 ran 32 %
+// slower, so the 256-wide tile trades k-block depth for stages.
 template <int BN>
 struct Variant {
-    static constexpr int kStages = BN == 256 ? 2 : 3;
+    static constexpr int kBK = BN == 256 ? 16 : 32;
+    static constexpr int kStages = BN == 256 ? 4 : 3;
     static constexpr int kThreads = tf32x3_threads(BN);
     static constexpr size_t kSmem =
-        static_cast<size_t>(kStages) * (2 * BM * BK * 4 + 2 * BN * BK * 4) + 1024 +
+        static_cast<size_t>(kStages) * (2 * BM * kBK * 4 + 2 * BN * kBK * 4) + 1024 +
         (BN == 128 ? static_cast<size_t>(4) * kStageFloats * 4 : 0);   // + epilogue staging
 };
 
-// rows x K fp32 matrix with row pitch Kp floats; boxes of 32 (K) x box_rows with
-// the 128-byte swizzle the UMMA descriptors expect.
-bool encode_kmajor(CUtensorMap* tm, const float* base, int rows, int K, int Kp, int box_rows) {
-    return encode_fp32_2d(tm, base, rows, K, Kp, BK, box_rows, /*swizzle128=*/true);
+__host__ __device__ constexpr int bk_for(int bn) { return bn == 256 ? 16 : 32; }
+
+// rows x K fp32 matrix with row pitch Kp floats; boxes of bk (K) x box_rows with
+// the swizzle the UMMA descriptors expect for bk-float rows.
+bool encode_kmajor(CUtensorMap* tm, const float* base, int rows, int K, int Kp, int bk,
+                   int box_rows) {
+    return encode_fp32_2d(tm, base, rows, K, Kp, bk, box_rows, bk * 4);
 }
 
 size_t region_floats(long long rows, int Kp) {
@@ -568,7 +581,7 @@ GemmArgs tf32x3_plan(int M, int N, int K, int bn, int sms, int schedule, SchedSi
     s.M = M;
     s.N = N;
     s.K = K;
-    *z = plan_schedule(s, tc::BM, bn, tc::BK, sms, 1, schedule);
+    *z = plan_schedule(s, tc::BM, bn, tc::bk_for(bn), sms, 1, schedule);
     return s;
 }
 
@@ -578,9 +591,10 @@ struct TcChoice {
 
 // Tile width (128 or 256) and schedule (1: data-parallel only, 0: stream-K on a
 // partial last wave or when tiles are fewer than SMs) with the smaller estimated
-// time: the k-blocks of the busiest CTA, a 256-wide k-block counting 1.9
-// 128-wide ones (each MMA re-reads A for twice the columns, about 5 % faster per
-// column), plus, when tiles are split, 8 k-blocks for the reduction launch and,
+// time: the k-blocks of the busiest CTA (128-wide: 32 deep, 256-wide: 16 deep), a
+// 256-wide 16-deep k-block counting 0.8 128-wide 32-deep ones (measured at 4096^3:
+// half the K, twice the columns, the A tile re-read for twice the columns and a
+// four-stage ring), plus, when tiles are split, 8 k-blocks for the reduction launch and,
 // per 128 columns of split tile, 0.12 (128-wide: staged, coalesced partial
 // stores) or 0.3 (256-wide: a row per lane) for writing and re-reading its
 // partials (fitted to measured times at 1024^3 .. 8192^3 and the ragged and
@@ -610,7 +624,7 @@ TcChoice tf32x3_choice(int M, int N, int K, int sms) {
             const double split_cost =
                 s.sk_tiles > 0 ? 8.0 + (bn == 256 ? 0.3 : 0.12) * s.sk_tiles * (bn / 128) : 0.0;
             const double t =
-                static_cast<double>(dp_per * s.KT + sk_per) * (bn == 256 ? 1.9 : 1.0) + split_cost;
+                static_cast<double>(dp_per * s.KT + sk_per) * (bn == 256 ? 0.8 : 1.0) + split_cost;
             if (best_t < 0.0 || t < best_t) {
                 best_t = t;
                 best = TcChoice{bn, sched};
@@ -692,7 +706,7 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tf32x3_kernel<BN, V::kStages, kChunkBlocks>,
+        attr_err = cudaFuncSetAttribute(tf32x3_kernel<BN, V::kBK, V::kStages>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(V::kSmem));
     });
@@ -701,10 +715,10 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
         return SGEMM_ERR_LAUNCH;
     }
     Params p{};
-    if (!encode_kmajor(&p.tm_ahi, L.ahi, M, K, Kp, BM) ||
-        !encode_kmajor(&p.tm_alo, L.alo, M, K, Kp, BM) ||
-        !encode_kmajor(&p.tm_bhi, L.bhi, N, K, Kp, BN) ||
-        !encode_kmajor(&p.tm_blo, L.blo, N, K, Kp, BN)) {
+    if (!encode_kmajor(&p.tm_ahi, L.ahi, M, K, Kp, V::kBK, BM) ||
+        !encode_kmajor(&p.tm_alo, L.alo, M, K, Kp, V::kBK, BM) ||
+        !encode_kmajor(&p.tm_bhi, L.bhi, N, K, Kp, V::kBK, BN) ||
+        !encode_kmajor(&p.tm_blo, L.blo, N, K, Kp, V::kBK, BN)) {
         set_last_error_message("tf32x3: cuTensorMapEncodeTiled failed");
         return SGEMM_ERR_LAUNCH;
     }
@@ -722,7 +736,7 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
     p.s.epi = (beta != 0.0f) ? kEpiAlphaBeta : (alpha != 1.0f ? kEpiAlpha : kEpiPlain);
     p.s.ws_partial = L.partial;
     p.s.status = status_word_ptr();
-    tf32x3_kernel<BN, V::kStages, kChunkBlocks><<<p.s.grid, V::kThreads, V::kSmem, stream>>>(p);
+    tf32x3_kernel<BN, V::kBK, V::kStages><<<p.s.grid, V::kThreads, V::kSmem, stream>>>(p);
     *launches = 1;
     if (cudaGetLastError() != cudaSuccess) {
         set_last_error_message("tf32x3: GEMM kernel failed to launch");
@@ -752,7 +766,7 @@ int tf32x3_query(int M, int N, int K, int sms, sgemm_config* out) {
     const bool wide = bn == 256;
     out->bm = tc::BM;
     out->bn = bn;
-    out->bk = tc::BK;
+    out->bk = tc::bk_for(bn);
     out->wm = 32;
     out->wn = 128;
     out->tm = 1;
