@@ -539,7 +539,9 @@ __global__ void __launch_bounds__(256) split_kernel(
 // about 192 KB of shared memory: 128 columns with 32-deep k-blocks and 3 stages
 // (64 KB each), 256 columns with 16-deep k-blocks and 4 stages (48 KB each).
 // The pipeline depth matters: 128 columns with 2 stages instead of 3 ran 32 %
-// slower, so the 256-wide tile trades k-block depth for stages.
+// slower, so the 256-wide tile trades k-block depth for stages.  The 128-wide
+// tile with 16-deep k-blocks and 6 stages ran 29 % slower than with 32-deep
+// blocks and 3: its k-blocks then hold too little MMA work per barrier round.
 template <int BN>
 struct Variant {
     static constexpr int kBK = BN == 256 ? 16 : 32;
