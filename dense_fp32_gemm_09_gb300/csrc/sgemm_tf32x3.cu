@@ -598,7 +598,7 @@ struct TcChoice {
 // half the K, twice the columns, the A tile re-read for twice the columns and a
 // four-stage ring), plus, when tiles are split, 8 k-blocks for the reduction launch and,
 // per 128 columns of split tile, 0.12 (128-wide: staged, coalesced partial
-// stores) or 0.3 (256-wide: a row per lane) for writing and re-reading its
+// stores) or 0.55 (256-wide: a row per lane) for writing and re-reading its
 // partials (fitted to measured times at 1024^3 .. 8192^3 and the ragged and
 // tall shapes).
 // SGEMM_TF32X3_BN and SGEMM_TF32X3_SCHEDULE (0 auto, 1 data-parallel, 2
@@ -624,7 +624,7 @@ TcChoice tf32x3_choice(int M, int N, int K, int sms) {
             const long long dp_per = (static_cast<long long>(s.dp_tiles) + s.grid - 1) / s.grid;
             const long long sk_per = (s.sk_iters + s.grid - 1) / s.grid;
             const double split_cost =
-                s.sk_tiles > 0 ? 8.0 + (bn == 256 ? 0.3 : 0.12) * s.sk_tiles * (bn / 128) : 0.0;
+                s.sk_tiles > 0 ? 8.0 + (bn == 256 ? 0.55 : 0.12) * s.sk_tiles * (bn / 128) : 0.0;
             const double t =
                 static_cast<double>(dp_per * s.KT + sk_per) * (bn == 256 ? 0.8 : 1.0) + split_cost;
             if (best_t < 0.0 || t < best_t) {
