@@ -220,10 +220,20 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
     return find_entry(name);
 }
 
+// Time to store one BM x BN tile, in BK-deep slices of the same tile.  A slice
+// is BM*BN*BK FMAs at about 100 per clock per SM; a store moves BM*BN*4 bytes at
+// about 32 bytes per clock per SM (both measured on the 128 x 256 kernels, and
+// both shared alike when several CTAs sit on one SM), so the ratio is ~12 / BK.
+double store_cost_slices(const KernelEntry& e) { return 12.0 / e.bk; }
+
 // schedule: 0 automatic, 1 data-parallel only, 2 stream-K whenever possible.
+// SGEMM_SK_GAP=<n> asks for that stream-K gap where it is allowed.
 void make_schedule(int sms, int occ, int entry, int schedule, Plan& p) {
     const KernelEntry& e = table()[entry];
-    const SchedSizes z = plan_schedule(p.args, e.bm, e.bn, e.bk, sms, occ, schedule);
+    int forced_gap = -1;
+    if (const char* g = std::getenv("SGEMM_SK_GAP")) forced_gap = std::atoi(g);
+    const SchedSizes z = plan_schedule(p.args, e.bm, e.bn, e.bk, sms, occ, schedule,
+                                       store_cost_slices(e), forced_gap < 0 ? -1 : forced_gap);
     p.ctas_per_sm = occ;
     p.split = z.split;
     p.ws_partial_bytes = z.partial_bytes;
@@ -616,6 +626,7 @@ void fill_config(const Plan& p, sgemm_config* out) {
     out->sk_tiles = p.args.sk_tiles;
     out->ctas_per_sm = p.ctas_per_sm;
     out->fma2 = e.fma2;
+    out->sk_gap = p.args.sk_gap;
 }
 
 // Walks every CTA's flat slice list exactly as the kernel does and checks the
@@ -662,7 +673,7 @@ int check_schedule(const Plan& p, char* why, size_t why_len) {
                                        static_cast<long long>(i % KT));
     for (int t = 0; t < a.sk_tiles; ++t) {
         const long long tb = static_cast<long long>(t) * KT;
-        const int g0 = sk_owner(tb, G, a.sk_iters), g1 = sk_owner(tb + KT - 1, G, a.sk_iters);
+        const int g0 = sk_owner(a, tb), g1 = sk_owner(a, tb + KT - 1);
         if (contrib[t] == 0) {
             if (g0 != g1) return fail("whole split tile with several owners", t, g1 - g0);
             continue;
@@ -670,7 +681,7 @@ int check_schedule(const Plan& p, char* why, size_t why_len) {
         if (contrib[t] != g1 - g0 + 1) return fail("contributor count", t, contrib[t]);
         if (contrib[t] > kMaxSplit) return fail("too many contributors", t, contrib[t]);
         for (int gg = g0; gg <= g1; ++gg) {
-            const int sl = t - static_cast<int>((a.sk_iters * gg / G) / KT);
+            const int sl = t - static_cast<int>(sk_begin(a, gg) / KT);
             if (sl < 0 || sl > 1) return fail("reduction slot out of range", t, gg);
         }
     }

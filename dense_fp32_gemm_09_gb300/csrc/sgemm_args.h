@@ -26,6 +26,7 @@ struct GemmArgs {
     int dp_tiles;          // tiles [0, dp_tiles) are done whole by one CTA each
     int sk_tiles;          // tiles [dp_tiles, dp_tiles + sk_tiles) are split over CTAs
     long long sk_iters;    // sk_tiles * KT: k-tiles shared out over the G CTAs
+    int sk_gap;            // virtual k-tiles counted between split tiles (sgemm_sched.cuh)
     int group_m;           // tile rasterisation: tile rows per group
 
     float* ws_partial;     // [G][2][BM*BN] partial tiles of split tiles

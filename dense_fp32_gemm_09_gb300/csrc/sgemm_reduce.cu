@@ -26,14 +26,14 @@ __global__ void __launch_bounds__(kReduceThreads) sk_reduce_kernel(const GemmArg
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.x / chunks, part = blockIdx.x - t * chunks;
     const long long tb = static_cast<long long>(t) * a.KT;
-    const int g0 = sk_owner(tb, a.grid, a.sk_iters);
-    const int g1 = sk_owner(tb + a.KT - 1, a.grid, a.sk_iters);
+    const int g0 = sk_owner(a, tb);
+    const int g1 = sk_owner(a, tb + a.KT - 1);
     const int n = g1 - g0 + 1;  // contributors, in increasing k order
     if (n <= 1) return;         // one CTA held the whole K range and stored the tile itself
     const long long tile_floats = static_cast<long long>(bm) * bn;
     for (int i = threadIdx.x; i < n; i += kReduceThreads) {
         const int gg = g0 + i;
-        const int slot = t - static_cast<int>((a.sk_iters * gg / a.grid) / a.KT);
+        const int slot = t - static_cast<int>(sk_begin(a, gg) / a.KT);
         s_src[i] = reinterpret_cast<const float4*>(
             a.ws_partial + (static_cast<long long>(gg) * 2 + slot) * tile_floats);
     }

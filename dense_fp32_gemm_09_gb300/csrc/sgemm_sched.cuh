@@ -3,10 +3,16 @@
 // The C tiles are numbered in a grouped raster order.  Tiles [0, dp_tiles) are
 // data-parallel: CTA g computes tiles g, g+G, g+2G, ... over their whole K
 // range.  The remaining sk_tiles tiles are split by k-slices: their
-// sk_iters = sk_tiles * KT slices are cut into G contiguous ranges
-// [floor(g*I/G), floor((g+1)*I/G)), one per CTA (stream-K).  A CTA walks its
-// data-parallel slices first and then its stream-K range as one flat list, so
-// its copy pipeline runs on across tile boundaries.
+// sk_iters = sk_tiles * KT slices are cut into G contiguous ranges, one per CTA
+// (stream-K).  A CTA walks its data-parallel slices first and then its
+// stream-K range as one flat list, so its copy pipeline runs on across tile
+// boundaries.
+//
+// The ranges are equal in a count that may include sk_gap "virtual" slices
+// after every split tile but the last.  No CTA computes those; they stand for
+// the time a CTA spends storing one more partial tile, so that a range which
+// crosses a tile boundary (and ends in two partial-tile stores) holds fewer
+// real slices.  sk_gap = 0 gives the plain equal split of sk_iters.
 #pragma once
 
 #include <stddef.h>
@@ -23,6 +29,31 @@ struct CtaWork {
     long long u0, u1, dp_iters, total, sk_iters;
 };
 
+// Stream-K partition.  Split-tile slice u = t*KT + k sits at virtual position
+// v = u + (u / KT) * sk_gap; there are V = sk_iters + (sk_tiles - 1) * sk_gap
+// positions, and CTA g owns the real slices with v in [floor(gV/G), floor((g+1)V/G)).
+__host__ __device__ __forceinline__ long long sk_virtual_total(const GemmArgs& a) {
+    return a.sk_tiles > 0 ? a.sk_iters + static_cast<long long>(a.sk_tiles - 1) * a.sk_gap : 0;
+}
+
+// First real slice at or after virtual position v.
+__host__ __device__ __forceinline__ long long sk_real_at(long long v, int KT, int gap) {
+    const long long P = static_cast<long long>(KT) + gap, t = v / P, k = v - t * P;
+    return k >= KT ? (t + 1) * KT : t * KT + k;
+}
+
+// First slice of CTA g's stream-K range; g = G gives sk_iters.
+__host__ __device__ __forceinline__ long long sk_begin(const GemmArgs& a, int g) {
+    return sk_real_at(sk_virtual_total(a) * g / a.grid, a.KT, a.sk_gap);
+}
+
+// The CTA whose range holds slice u: the g with floor(gV/G) <= v < floor((g+1)V/G),
+// which is floor(((v + 1) G - 1) / V).
+__host__ __device__ __forceinline__ int sk_owner(const GemmArgs& a, long long u) {
+    const long long v = u + (u / a.KT) * a.sk_gap;
+    return static_cast<int>(((v + 1) * a.grid - 1) / sk_virtual_total(a));
+}
+
 __host__ __device__ __forceinline__ CtaWork make_work(const GemmArgs& a, int g) {
     CtaWork w;
     w.g = g;
@@ -31,21 +62,16 @@ __host__ __device__ __forceinline__ CtaWork make_work(const GemmArgs& a, int g) 
     w.dp_tiles = a.dp_tiles;
     w.n_dp = (w.g < a.dp_tiles) ? (a.dp_tiles - 1 - w.g) / w.G + 1 : 0;
     w.sk_iters = a.sk_iters;
-    w.u0 = a.sk_iters * w.g / w.G;
-    w.u1 = a.sk_iters * (w.g + 1) / w.G;
+    w.u0 = a.sk_tiles > 0 ? sk_begin(a, w.g) : 0;
+    w.u1 = a.sk_tiles > 0 ? sk_begin(a, w.g + 1) : 0;
     w.dp_iters = static_cast<long long>(w.n_dp) * w.KT;
     w.total = w.dp_iters + (w.u1 - w.u0);
     return w;
 }
 
-// The CTA whose stream-K range holds shared k-slice u:
-// ranges are [floor(g*I/G), floor((g+1)*I/G)), so it is floor(((u+1)G - 1) / I).
-__host__ __device__ __forceinline__ int sk_owner(long long u, int G, long long I) {
-    return static_cast<int>(((u + 1) * G - 1) / I);
-}
-
 // Partial-tile slot (0 or 1) CTA w uses for split tile t: a CTA's stream-K range
-// is shorter than one tile's K range, so it touches at most two split tiles.
+// is shorter than one tile's K range plus one gap, so it touches at most two
+// split tiles.
 __host__ __device__ __forceinline__ int sk_slot(const CtaWork& w, int t) {
     return t - static_cast<int>(w.u0 / w.KT);
 }
@@ -109,11 +135,58 @@ struct SchedSizes {
     size_t partial_bytes = 0;   // workspace bytes of partial tiles
 };
 
+constexpr int kMaxSkGap = 3;   // largest gap the automatic choice tries
+
+// Longest CTA of the current schedule, in k-slices, when storing a tile (whole
+// or partial) costs `store` slices: the quantity the gap choice minimises.
+inline double sk_critical_path(const GemmArgs& a, double store) {
+    double worst = 0.0;
+    const int extra = a.dp_tiles % a.grid;   // CTAs [0, extra) hold one more whole tile
+    const int n_dp_lo = a.dp_tiles / a.grid;
+    long long u0 = a.sk_tiles > 0 ? sk_begin(a, 0) : 0;
+    for (int g = 0; g < a.grid; ++g) {
+        const long long u1 = a.sk_tiles > 0 ? sk_begin(a, g + 1) : 0;
+        const int n_dp = n_dp_lo + (g < extra ? 1 : 0);
+        const long long pieces = u1 > u0 ? (u1 - 1) / a.KT - u0 / a.KT + 1 : 0;
+        const double c = n_dp * (a.KT + store) + static_cast<double>(u1 - u0) + pieces * store;
+        if (c > worst) worst = c;
+        u0 = u1;
+    }
+    return worst;
+}
+
+// Gap for the stream-K partition (see the top of this file): the smallest one in
+// [0, kMaxSkGap] with the shortest critical path, among those that leave every
+// CTA at least one real slice.  forced >= 0 asks for that gap, if it is allowed.
+inline int choose_sk_gap(GemmArgs& a, double store, int forced) {
+    if (a.sk_tiles <= 1) return 0;
+    int best = 0;
+    double best_cost = 0.0;
+    for (int gap = 0; gap <= (forced >= 0 ? forced : kMaxSkGap); ++gap) {
+        a.sk_gap = gap;
+        // Ranges of at least gap + 1 positions always hold a real slice.
+        if (sk_virtual_total(a) / a.grid < gap + 1) break;
+        if (forced >= 0) {
+            if (gap == forced) best = gap;
+            continue;
+        }
+        const double c = sk_critical_path(a, store);
+        if (gap == 0 || c < best_cost - 1e-9) {
+            best = gap;
+            best_cost = c;
+        }
+    }
+    return best;
+}
+
 // Fills the schedule fields of `a` (a.M, a.N, a.K set) for BM x BN x BK tiles on
 // `sms` SMs holding `occ` CTAs each.  schedule: 0 automatic, 1 data-parallel
 // only, 2 stream-K on any partial wave that has at least one k-slice per CTA.
+// store_slices: cost of storing one tile in k-slices (0: equal stream-K ranges,
+// no gap); forced_gap >= 0 overrides the gap choice where it is allowed.
 inline SchedSizes plan_schedule(GemmArgs& a, int bm, int bn, int bk, int sms, int occ,
-                                int schedule) {
+                                int schedule, double store_slices = 0.0,
+                                int forced_gap = -1) {
     a.tiles_m = (a.M + bm - 1) / bm;
     a.tiles_n = (a.N + bn - 1) / bn;
     a.KT = (a.K + bk - 1) / bk;
@@ -157,11 +230,14 @@ inline SchedSizes plan_schedule(GemmArgs& a, int bm, int bn, int bk, int sms, in
         a.dp_tiles = static_cast<int>(dp);
         a.sk_tiles = static_cast<int>(sk);
         a.sk_iters = sk * a.KT;
+        a.sk_gap = 0;
+        if (store_slices > 0.0 || forced_gap >= 0)
+            a.sk_gap = choose_sk_gap(a, store_slices, forced_gap);
         z.split = 1;
         for (long long t = 0; t < sk; ++t) {
             const long long tb = t * a.KT, te = tb + a.KT - 1;
-            const int g0 = sk_owner(tb, static_cast<int>(G), a.sk_iters);
-            const int g1 = sk_owner(te, static_cast<int>(G), a.sk_iters);
+            const int g0 = sk_owner(a, tb);
+            const int g1 = sk_owner(a, te);
             if (g1 - g0 + 1 > z.split) z.split = g1 - g0 + 1;
         }
         // The reduction handles at most kMaxSplit contributors per tile: use fewer

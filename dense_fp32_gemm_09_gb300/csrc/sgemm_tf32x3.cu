@@ -785,6 +785,7 @@ int tf32x3_query(int M, int N, int K, int sms, sgemm_config* out) {
     out->ctas_per_sm = 1;
     out->fma2 = 0;
     out->packed = 0;
+    out->sk_gap = s.sk_gap;
     return SGEMM_OK;
 }
 

@@ -82,6 +82,8 @@ typedef struct {
     int ctas_per_sm;       /* resident CTAs per SM for this kernel */
     int fma2;              /* 1: packed fma.rn.f32x2 micro-kernel */
     int packed;            /* sgemm_run copies A (bit 0) / B (bit 1) to aligned buffers first */
+    int sk_gap;            /* stream-K: k-slices of store time counted between split tiles
+                              when the K ranges are shared out (0: equal ranges) */
 } sgemm_config;
 
 /* C = A.B on `stream`.  One kernel launch, plus a second, short reduction launch

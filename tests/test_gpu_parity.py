@@ -231,6 +231,35 @@ def test_stream_k_matches_data_parallel_within_tolerance(cuda, oracle_mod):
             assert np.max(np.abs(C - ref)) <= tolerance(A, B)
 
 
+@pytest.mark.parametrize("gap", ["0", "1", "2", "3"])
+def test_stream_k_gap_parity(cuda, oracle_mod, monkeypatch, gap):
+    """Stream-K ranges with 0..3 placeholder slices between split tiles: every
+    kernel, on shapes whose tiles are all split or whose last wave is, matches the
+    oracle, writes nothing outside C, repeats bit for bit, and reports the gap."""
+    torch = cuda
+    monkeypatch.setenv("SGEMM_SK_GAP", gap)
+    used = 0
+    for (M, N, K) in [(1024, 1024, 1024), (700, 900, 2500), (1001, 517, 1999)]:
+        A, B = random_pair(M, N, K, seed=M + N + K)
+        ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+        dA = padded(torch, A, (-K) % 4 + 4)
+        dB = padded(torch, B, (-N) % 4 + 4)
+        for k in kernel_table():
+            buf, C = canaried(torch, M, N, ldc_pad=(-N) % 4 + 4)
+            sgemm(dA, dB, out=C, kernel_id=k["kernel_id"], schedule=2)
+            first = C.clone()
+            sgemm(dA, dB, out=C, kernel_id=k["kernel_id"], schedule=2)
+            torch.cuda.synchronize()
+            check_canary(buf, M, N)
+            assert torch.equal(first, C), (k["name"], gap)
+            err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+            assert err <= tolerance(A, B), (k["name"], gap, (M, N, K), err)
+        cfg = sgemm_query_config(M, N, K, dA.stride(0), dB.stride(0), N, dA.data_ptr(),
+                                 dB.data_ptr(), None)
+        used += cfg["sk_gap"] == int(gap)
+    assert used > 0
+
+
 def test_caller_workspace_entry_point(cuda, oracle_mod):
     torch = cuda
     from dense_fp32_gemm_09_gb300 import check, sgemm_run_ws, sgemm_workspace_size

@@ -68,3 +68,98 @@ def test_schedule_of_operands_past_2_31_elements(lib, M, N, K):
             cfg = _cfg()
             rc = lib.sgemm_schedule_check(M, N, K, kid, sms, occ, 0, ctypes.byref(cfg))
             assert rc == 0, (kid, sms, occ, lib.sgemm_last_error())
+
+
+# --------------------------------------------------------------------------
+# stream-K gap: split tiles separated by virtual slices that stand for the
+# cost of one more partial-tile store
+# --------------------------------------------------------------------------
+
+
+def _kid(lib, name):
+    return [lib.sgemm_kernel_name(i).decode()
+            for i in range(lib.sgemm_num_kernels())].index(name)
+
+
+@pytest.mark.parametrize("gap", [1, 2, 3])
+@pytest.mark.parametrize("schedule", [0, 2])
+def test_forced_gap_covers_each_slice_once(lib, monkeypatch, gap, schedule):
+    monkeypatch.setenv("SGEMM_SK_GAP", str(gap))
+    n = lib.sgemm_num_kernels()
+    used = 0
+    for kid, (M, N, K), (sms, occ) in itertools.product(range(n), SHAPES, MACHINES):
+        cfg = _cfg()
+        rc = lib.sgemm_schedule_check(M, N, K, kid, sms, occ, schedule, ctypes.byref(cfg))
+        assert rc == 0, (kid, M, N, K, sms, occ, gap, lib.sgemm_last_error())
+        assert cfg.sk_gap in (0, gap)
+        used += cfg.sk_gap == gap
+    assert used > 0
+
+
+def _brute_force_critical_path(T_sk, KT, G, gap, dp_tiles, store):
+    """Longest CTA (k-slices plus `store` per tile stored) when the split tiles'
+    slices, each followed by `gap` placeholder positions except the last tile,
+    are dealt out to G CTAs as equal ranges of positions.  None: some CTA would
+    get no real slice."""
+    pos = []
+    for t in range(T_sk):
+        pos += [t] * KT
+        if t < T_sk - 1:
+            pos += [None] * gap
+    V = len(pos)
+    if V // G < gap + 1:
+        return None
+    worst = 0.0
+    for g in range(G):
+        real = [t for t in pos[g * V // G:(g + 1) * V // G] if t is not None]
+        assert real, "a CTA without a real slice"
+        n_dp = len(range(g, dp_tiles, G))
+        worst = max(worst, n_dp * (KT + store) + len(real) + len(set(real)) * store)
+    return worst
+
+
+@pytest.mark.parametrize("M,N,K,name,occ", [
+    (1024, 1024, 1024, "128x256x32_t8x16_s4_f2_tma", 1),
+    (2048, 2048, 2048, "128x256x64_t8x16_s2_f2_v4", 1),
+    (4096, 4096, 4096, "128x256x64_t8x16_s2_f2_v4", 1),
+    (3001, 2047, 1999, "128x256x32_t8x16_s4_f2_tma", 1),
+    (16384, 64, 4096, "128x64x16_t16x8_s4_f2_v4", 4),
+    (256, 256, 256, "64x64x16_t8x8_s3_f2_v4", 4),
+    (1500, 1000, 3000, "128x128x32_t8x8_s3_f2_v4", 2),
+    (700, 900, 2500, "128x256x16_t8x16_s6_f2_v4", 1),
+])
+def test_gap_choice_minimises_the_critical_path(lib, monkeypatch, M, N, K, name, occ):
+    """The planner's gap is the smallest one with the shortest longest-CTA time,
+    the partition rebuilt here position by position."""
+    monkeypatch.delenv("SGEMM_SK_GAP", raising=False)
+    cfg = _cfg()
+    assert lib.sgemm_schedule_check(M, N, K, _kid(lib, name), 152, occ, 0,
+                                    ctypes.byref(cfg)) == 0
+    KT = -(-K // cfg.bk)
+    store = 12.0 / cfg.bk
+    dp = cfg.tiles - cfg.sk_tiles
+    best, best_cost = 0, None
+    if cfg.sk_tiles > 1:
+        for gap in range(4):
+            c = _brute_force_critical_path(cfg.sk_tiles, KT, cfg.grid, gap, dp, store)
+            if c is None:
+                break
+            if best_cost is None or c < best_cost - 1e-9:
+                best, best_cost = gap, c
+    assert cfg.sk_gap == best, (cfg.sk_gap, best)
+
+
+def test_gap_takes_a_store_off_the_1024_cube_critical_path(lib, monkeypatch):
+    """1024^3 on 128x256x32 tiles: 32 split tiles of 32 slices over 152 CTAs.  Equal
+    ranges give some CTA 7 slices and two partial stores; one placeholder slice per
+    boundary leaves 7 slices and one store at most."""
+    monkeypatch.delenv("SGEMM_SK_GAP", raising=False)
+    cfg = _cfg()
+    assert lib.sgemm_schedule_check(1024, 1024, 1024,
+                                    _kid(lib, "128x256x32_t8x16_s4_f2_tma"), 152, 1, 0,
+                                    ctypes.byref(cfg)) == 0
+    assert (cfg.grid, cfg.sk_tiles, cfg.sk_gap) == (152, 32, 1)
+    store = 12.0 / 32
+    c0 = _brute_force_critical_path(32, 32, 152, 0, 0, store)
+    c1 = _brute_force_critical_path(32, 32, 152, 1, 0, store)
+    assert c0 == pytest.approx(7 + 2 * store) and c1 == pytest.approx(7 + store)
