@@ -210,7 +210,11 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
     const long long tiles128 = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
     const char* name;
     if (v4 && N <= 64)
-        name = "128x64x16_t16x8_s4_f2_v4";
+        // Narrow C: 512-row tiles once M fills 8 of them, small tiles below.
+        name = M >= 4096 ? "512x64x32_t8x16_s2_f2_v4" : "64x64x16_t8x8_s3_f2_v4";
+    else if (v4 && N <= 128 && M >= 4096)
+        // A 256-wide tile would compute half its columns for nothing.
+        name = "256x128x64_t8x16_s2_f2_v4";
     else if (tiles128 * 4 < d.sms)
         name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
     else if (v4)

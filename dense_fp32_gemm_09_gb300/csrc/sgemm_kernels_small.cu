@@ -5,12 +5,18 @@ namespace sgemm {
 
 // FfmaCfg<BM, BN, BK, TM, TN, LR, WARPS_M, WARPS_N, STAGES, VEC, AK, FMA2, MINB>
 using Tall16x8 = FfmaCfg<128, 64, 16, 16, 8, 4, 2, 1, 4, 4, 4, true, 4>;
+// One 256-thread CTA per SM for narrow C (N <= 64): eight 64 x 64 warp tiles
+// stacked along M, 8 x 16 register tiles with 8 lane-rows.  With four 64-thread
+// CTAs per SM instead, the warp scheduler lets some CTAs run ahead and the SM
+// spends the last third of a 16384 x 64 x 4096 product short of warps.
+using Tall512K32 = FfmaCfg<512, 64, 32, 8, 16, 8, 8, 1, 2, 4, 4, true, 1>;
 using Small8x8 = FfmaCfg<64, 64, 16, 8, 8, 4, 2, 1, 3, 4, 4, true, 4>;
 using Small4x4 = FfmaCfg<64, 64, 16, 4, 4, 4, 4, 2, 3, 4, 4, false, 3>;
 using Small8x4 = FfmaCfg<64, 64, 16, 8, 4, 4, 2, 2, 3, 4, 4, true, 4>;
 
 static const KernelEntry kEntries[] = {
     make_entry<Tall16x8>("128x64x16_t16x8_s4_f2_v4"),
+    make_entry<Tall512K32>("512x64x32_t8x16_s2_f2_v4"),
     make_entry<Small8x8>("64x64x16_t8x8_s3_f2_v4"),
     make_entry<Small4x4>("64x64x16_t4x4_s3_f1_v4"),
     make_entry<Small8x4>("64x64x16_t8x4_s3_f2_v4"),

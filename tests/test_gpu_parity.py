@@ -386,6 +386,31 @@ def test_query_config_matches_bench_choice(cuda):
     assert small["packed"] == 0 and small["vec"] == 1   # too small to be worth copying
 
 
+@pytest.mark.parametrize("M,N,K,name", [
+    (16384, 64, 4096, "512x64x32_t8x16_s2_f2_v4"),
+    (4096, 36, 1000, "512x64x32_t8x16_s2_f2_v4"),
+    (2048, 64, 4096, "64x64x16_t8x8_s3_f2_v4"),
+    (8192, 128, 4096, "256x128x64_t8x16_s2_f2_v4"),
+    (8192, 96, 4096, "256x128x64_t8x16_s2_f2_v4"),
+    (4096, 4096, 4096, "128x256x64_t8x16_s2_f2_v4"),
+])
+def test_narrow_c_tile_choice(cuda, M, N, K, name):
+    """Narrow C gets tiles no wider than it: 512 x 64 for N <= 64 once M fills eight
+    of them, 256 x 128 for N <= 128."""
+    assert sgemm_query_config(M, N, K)["name"] == name
+
+
+def test_narrow_c_parity(cuda, oracle_mod):
+    """The narrow-C choices above, full products against the oracle."""
+    torch = cuda
+    for (M, N, K) in [(4100, 61, 777), (4096, 128, 512), (5000, 100, 300)]:
+        A, B = random_pair(M, N, K, seed=M + N)
+        C = sgemm(A.cuda(), B.cuda())
+        ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+        err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+        assert err <= tolerance(A, B), ((M, N, K), err)
+
+
 def test_launch_counter_counts(cuda):
     torch = cuda
     from dense_fp32_gemm_09_gb300 import launch_count
