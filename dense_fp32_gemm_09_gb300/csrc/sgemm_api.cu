@@ -218,7 +218,7 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
     else if (tiles128 * 4 < d.sms)
         name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
     else if (v4)
-        name = K >= 2048 ? "128x256x64_t8x16_s2_f2_v4" : "128x256x32_t8x16_s4_f2_tma";
+        name = K >= 2048 ? "256x128x64_t8x16_s2_f2_v4" : "128x256x32_t8x16_s4_f2_tma";
     else
         name = "128x256x32_t8x16_s3_f2_v1";
     return find_entry(name);
@@ -231,13 +231,16 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
 double store_cost_slices(const KernelEntry& e) { return 12.0 / e.bk; }
 
 // schedule: 0 automatic, 1 data-parallel only, 2 stream-K whenever possible.
-// SGEMM_SK_GAP=<n> asks for that stream-K gap where it is allowed.
+// SGEMM_SK_GAP=<n> asks for that stream-K gap where it is allowed;
+// SGEMM_GROUP_M=<n> sets the raster group height (tuning).
 void make_schedule(int sms, int occ, int entry, int schedule, Plan& p) {
     const KernelEntry& e = table()[entry];
-    int forced_gap = -1;
+    int forced_gap = -1, group_m = 0;
     if (const char* g = std::getenv("SGEMM_SK_GAP")) forced_gap = std::atoi(g);
+    if (const char* g = std::getenv("SGEMM_GROUP_M")) group_m = std::max(0, std::atoi(g));
     const SchedSizes z = plan_schedule(p.args, e.bm, e.bn, e.bk, sms, occ, schedule,
-                                       store_cost_slices(e), forced_gap < 0 ? -1 : forced_gap);
+                                       store_cost_slices(e), forced_gap < 0 ? -1 : forced_gap,
+                                       group_m);
     p.ctas_per_sm = occ;
     p.split = z.split;
     p.ws_partial_bytes = z.partial_bytes;

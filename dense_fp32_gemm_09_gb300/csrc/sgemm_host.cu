@@ -78,7 +78,7 @@ int host_pipe(HostPipe** out) {
     return SGEMM_OK;
 }
 
-// Row panels for the host-buffer entry: fills rows[] (multiples of 128 but the
+// Row panels for the host-buffer entry: fills rows[] (multiples of 256 but the
 // last) and returns their number.  Large problems: 25 % of the rows (computed in
 // k-chunks as their inputs arrive), then 65 % in one efficient product, then a
 // last 10 % whose copy back is the only exposed tail (measured best of several
@@ -115,8 +115,10 @@ int host_panels(int M, int N, int K, int (&rows)[kMaxHostPanels]) {
     for (int i = 0; i < n_pct; ++i) total += pct[i];
     int n = 0, done = 0;
     for (int i = 0; i < n_pct && done < M; ++i) {
+        // Panels of whole 256-row tiles (two 128-row ones): a panel that ends
+        // inside a tile row computes the rest of that row for nothing.
         int r = static_cast<int>(static_cast<long long>(M) * pct[i] / total);
-        r = std::max(128, (r + 127) / 128 * 128);
+        r = std::max(256, (r + 128) / 256 * 256);
         if (i == n_pct - 1 || done + r > M) r = M - done;
         rows[n++] = r;
         done += r;

@@ -5,11 +5,13 @@
 namespace sgemm {
 
 // FfmaCfg<BM, BN, BK, TM, TN, LR, WARPS_M, WARPS_N, STAGES, VEC, AK, FMA2, MINB, PIPE>
-// One 256-thread CTA per SM with 8 x 16 register tiles (255 registers): the
+// One 256-thread CTA per SM with 8 x 16 register tiles (up to 255 registers): the
 // large-problem workhorses; BK = 64 halves the per-slice overhead when K is long.
-// The BK = 64 one double-buffers its fragments (A two k at a time): 1.2 % faster
-// at 2048^3 .. 8192^3 than single-buffered fragments four k at a time; on the
-// other entries the same change measured neutral or slower.
+// The 128 x 256 x 64 one double-buffers its fragments (A two k at a time): 1.2 %
+// faster at 2048^3 .. 8192^3 than single-buffered fragments four k at a time.
+// The 256 x 128 x 64 one, the same eight 32 x 128 warp tiles stacked along M and
+// fragments single-buffered, is 0.7 % faster still at those sizes (double-
+// buffering it measured slower); it serves aligned problems with K >= 2048.
 using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 2, true, 1, true>;
 using W256K32 = FfmaCfg<128, 256, 32, 8, 16, 4, 4, 2, 4, 4, 4, true, 1>;
 using W256K16 = FfmaCfg<128, 256, 16, 8, 16, 4, 4, 2, 6, 4, 4, true, 1>;

@@ -17,6 +17,8 @@
 
 #include <stddef.h>
 
+#include <cmath>
+
 #include "sgemm_args.h"
 
 namespace sgemm {
@@ -183,20 +185,28 @@ inline int choose_sk_gap(GemmArgs& a, double store, int forced) {
 // `sms` SMs holding `occ` CTAs each.  schedule: 0 automatic, 1 data-parallel
 // only, 2 stream-K on any partial wave that has at least one k-slice per CTA.
 // store_slices: cost of storing one tile in k-slices (0: equal stream-K ranges,
-// no gap); forced_gap >= 0 overrides the gap choice where it is allowed.
+// no gap); forced_gap >= 0 overrides the gap choice where it is allowed;
+// group_m > 0 sets the raster group height (0: chosen from the tile shape).
 inline SchedSizes plan_schedule(GemmArgs& a, int bm, int bn, int bk, int sms, int occ,
                                 int schedule, double store_slices = 0.0,
-                                int forced_gap = -1) {
+                                int forced_gap = -1, int group_m = 0) {
     a.tiles_m = (a.M + bm - 1) / bm;
     a.tiles_n = (a.N + bn - 1) / bn;
     a.KT = (a.K + bk - 1) / bk;
-    // 16 tile rows per raster group: a wave of ~152 tiles then spans about 16 rows
-    // x 9.5 columns rather than 8 rows x all columns, so each wave reads A rows
-    // and B columns in a ratio near the optimum (fewer repeated B reads from DRAM).
-    a.group_m = a.tiles_m < 16 ? a.tiles_m : 16;
     const long long T = static_cast<long long>(a.tiles_m) * a.tiles_n;
     long long Gmax = static_cast<long long>(sms) * occ;
     if (Gmax > kMaxSkTiles) Gmax = kMaxSkTiles;
+    // Raster groups of group_m tile rows.  A wave of G tiles spanning r tile rows
+    // and G/r columns reads r*BM rows of A and (G/r)*BN columns of B per k; that
+    // is least for r = sqrt(G*BN/BM).  group_m is the power of two nearest to it
+    // (16 for 128 x 256 tiles on 152 SMs, 8 for 256 x 128), so waves repeat
+    // fewer DRAM reads of either operand.
+    if (group_m <= 0) {
+        const double r = std::sqrt(static_cast<double>(Gmax) * bn / bm);
+        group_m = 1;
+        while (group_m < 4096 && group_m * 1.4142135623730951 < r) group_m *= 2;
+    }
+    a.group_m = a.tiles_m < group_m ? a.tiles_m : group_m;
 
     long long G, dp, sk;
     if (T >= Gmax) {
