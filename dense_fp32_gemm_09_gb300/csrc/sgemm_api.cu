@@ -218,7 +218,7 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
     else if (tiles128 * 4 < d.sms)
         name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
     else if (v4)
-        name = K >= 2048 ? "256x128x64_t8x16_s2_f2_v4" : "128x256x32_t8x16_s4_f2_tma";
+        name = K >= 2048 ? "256x128x64_t8x16_s2_f2_v4" : "256x128x32_t8x16_s4_f2_v4";
     else
         name = "128x256x32_t8x16_s3_f2_v1";
     return find_entry(name);

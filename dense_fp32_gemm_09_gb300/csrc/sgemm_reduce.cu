@@ -21,9 +21,10 @@ constexpr int kBatch = 8;
 __global__ void __launch_bounds__(kReduceThreads) sk_reduce_kernel(const GemmArgs a, int bm,
                                                                    int bn, int chunks) {
     __shared__ const float4* s_src[kMaxSplit];
-    // Launched as a programmatic dependent of the main kernel: everything above
-    // this wait overlaps the main kernel's tail; nothing it wrote is read before.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Launched as a programmatic dependent of the main kernel.  The contributor
+    // list below depends on the launch arguments only, so it is worked out while
+    // the main kernel finishes; griddepcontrol.wait comes before the first read
+    // of anything that kernel wrote.
     const int t = blockIdx.x / chunks, part = blockIdx.x - t * chunks;
     const long long tb = static_cast<long long>(t) * a.KT;
     const int g0 = sk_owner(a, tb);
@@ -40,6 +41,7 @@ __global__ void __launch_bounds__(kReduceThreads) sk_reduce_kernel(const GemmArg
     __syncthreads();
     int m0, n0;
     tile_origin(a, a.dp_tiles + t, bm, bn, m0, n0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n4 = bm * bn / 4;  // float4 per tile
     const int per = (n4 + chunks - 1) / chunks;
     const int e_end = min(n4, (part + 1) * per);

@@ -44,16 +44,27 @@ __host__ __device__ __forceinline__ long long sk_real_at(long long v, int KT, in
     return k >= KT ? (t + 1) * KT : t * KT + k;
 }
 
+// The gap > 0 forms of the two lookups below, kept out of line: 64-bit
+// divisions are long instruction sequences on the GPU, and the kernels' prologue
+// (fetched cold after an L2 flush) should carry only the equal split's one.
+inline __host__ __device__ __noinline__ long long sk_begin_gap(const GemmArgs& a, int g) {
+    return sk_real_at(sk_virtual_total(a) * g / a.grid, a.KT, a.sk_gap);
+}
+inline __host__ __device__ __noinline__ int sk_owner_gap(const GemmArgs& a, long long u) {
+    const long long v = u + (u / a.KT) * a.sk_gap;
+    return static_cast<int>(((v + 1) * a.grid - 1) / sk_virtual_total(a));
+}
+
 // First slice of CTA g's stream-K range; g = G gives sk_iters.
 __host__ __device__ __forceinline__ long long sk_begin(const GemmArgs& a, int g) {
-    return sk_real_at(sk_virtual_total(a) * g / a.grid, a.KT, a.sk_gap);
+    return a.sk_gap == 0 ? a.sk_iters * g / a.grid : sk_begin_gap(a, g);
 }
 
 // The CTA whose range holds slice u: the g with floor(gV/G) <= v < floor((g+1)V/G),
 // which is floor(((v + 1) G - 1) / V).
 __host__ __device__ __forceinline__ int sk_owner(const GemmArgs& a, long long u) {
-    const long long v = u + (u / a.KT) * a.sk_gap;
-    return static_cast<int>(((v + 1) * a.grid - 1) / sk_virtual_total(a));
+    return a.sk_gap == 0 ? static_cast<int>(((u + 1) * a.grid - 1) / a.sk_iters)
+                         : sk_owner_gap(a, u);
 }
 
 __host__ __device__ __forceinline__ CtaWork make_work(const GemmArgs& a, int g) {
@@ -64,8 +75,8 @@ __host__ __device__ __forceinline__ CtaWork make_work(const GemmArgs& a, int g) 
     w.dp_tiles = a.dp_tiles;
     w.n_dp = (w.g < a.dp_tiles) ? (a.dp_tiles - 1 - w.g) / w.G + 1 : 0;
     w.sk_iters = a.sk_iters;
-    w.u0 = a.sk_tiles > 0 ? sk_begin(a, w.g) : 0;
-    w.u1 = a.sk_tiles > 0 ? sk_begin(a, w.g + 1) : 0;
+    w.u0 = sk_begin(a, w.g);       // 0 when no tile is split (sk_iters = 0, gap 0)
+    w.u1 = sk_begin(a, w.g + 1);
     w.dp_iters = static_cast<long long>(w.n_dp) * w.KT;
     w.total = w.dp_iters + (w.u1 - w.u0);
     return w;
@@ -145,9 +156,9 @@ inline double sk_critical_path(const GemmArgs& a, double store) {
     double worst = 0.0;
     const int extra = a.dp_tiles % a.grid;   // CTAs [0, extra) hold one more whole tile
     const int n_dp_lo = a.dp_tiles / a.grid;
-    long long u0 = a.sk_tiles > 0 ? sk_begin(a, 0) : 0;
+    long long u0 = sk_begin(a, 0);
     for (int g = 0; g < a.grid; ++g) {
-        const long long u1 = a.sk_tiles > 0 ? sk_begin(a, g + 1) : 0;
+        const long long u1 = sk_begin(a, g + 1);
         const int n_dp = n_dp_lo + (g < extra ? 1 : 0);
         const long long pieces = u1 > u0 ? (u1 - 1) / a.KT - u0 / a.KT + 1 : 0;
         const double c = n_dp * (a.KT + store) + static_cast<double>(u1 - u0) + pieces * store;
@@ -162,6 +173,24 @@ inline double sk_critical_path(const GemmArgs& a, double store) {
 // CTA at least one real slice.  forced >= 0 asks for that gap, if it is allowed.
 inline int choose_sk_gap(GemmArgs& a, double store, int forced) {
     if (a.sk_tiles <= 1) return 0;
+    // The search walks every CTA for each gap (microseconds of host time per
+    // call); its answer depends on these few numbers only, so each thread keeps
+    // the last answers for a handful of schedules.
+    struct Memo {
+        long long sk_iters;
+        int sk_tiles, KT, grid, dp_tiles, forced, gap;
+        double store;
+        bool used;
+    };
+    static thread_local Memo memo[16];
+    const unsigned slot = (static_cast<unsigned>(a.sk_tiles) * 2654435761u ^
+                           static_cast<unsigned>(a.KT) * 40503u ^
+                           static_cast<unsigned>(a.grid) * 97u ^
+                           static_cast<unsigned>(a.dp_tiles) * 13u) % 16u;
+    Memo& m = memo[slot];
+    if (m.used && m.sk_iters == a.sk_iters && m.sk_tiles == a.sk_tiles && m.KT == a.KT &&
+        m.grid == a.grid && m.dp_tiles == a.dp_tiles && m.forced == forced && m.store == store)
+        return m.gap;
     int best = 0;
     double best_cost = 0.0;
     for (int gap = 0; gap <= (forced >= 0 ? forced : kMaxSkGap); ++gap) {
@@ -178,6 +207,7 @@ inline int choose_sk_gap(GemmArgs& a, double store, int forced) {
             best_cost = c;
         }
     }
+    m = Memo{a.sk_iters, a.sk_tiles, a.KT, a.grid, a.dp_tiles, forced, best, store, true};
     return best;
 }
 

@@ -393,7 +393,7 @@ def test_query_config_matches_bench_choice(cuda):
     (8192, 128, 4096, "256x128x64_t8x16_s2_f2_v4"),
     (8192, 96, 4096, "256x128x64_t8x16_s2_f2_v4"),
     (4096, 4096, 4096, "256x128x64_t8x16_s2_f2_v4"),
-    (1024, 1024, 1024, "128x256x32_t8x16_s4_f2_tma"),
+    (1024, 1024, 1024, "256x128x32_t8x16_s4_f2_v4"),
 ])
 def test_narrow_c_tile_choice(cuda, M, N, K, name):
     """Narrow C gets tiles no wider than it: 512 x 64 for N <= 64 once M fills eight

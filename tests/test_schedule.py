@@ -126,6 +126,8 @@ def _brute_force_critical_path(T_sk, KT, G, gap, dp_tiles, store):
     (4096, 4096, 4096, "256x128x64_t8x16_s2_f2_v4", 1),
     (8192, 8192, 8192, "256x128x64_t8x16_s2_f2_v4", 1),
     (16384, 64, 4096, "512x64x32_t8x16_s2_f2_v4", 1),
+    (1024, 1024, 1024, "256x128x32_t8x16_s4_f2_v4", 1),
+    (3001, 2047, 1999, "256x128x32_t8x16_s4_f2_v4", 1),
     (3001, 2047, 1999, "128x256x32_t8x16_s4_f2_tma", 1),
     (16384, 64, 4096, "128x64x16_t16x8_s4_f2_v4", 4),
     (256, 256, 256, "64x64x16_t8x8_s3_f2_v4", 4),
