@@ -365,8 +365,18 @@ int launch(const Plan& p, cudaStream_t stream) {
     cfg.blockDim = dim3(static_cast<unsigned>(e.threads));
     cfg.dynamicSmemBytes = static_cast<size_t>(e.smem_bytes);
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    // Programmatic dependent launch: the kernel may start while the stream's
+    // previous kernel drains, and waits (griddepcontrol.wait) before touching
+    // global memory.  SGEMM_PDL=0 launches it plainly (tuning).
+    static const bool pdl = [] {
+        const char* v = std::getenv("SGEMM_PDL");
+        return v == nullptr || std::atoi(v) != 0;
+    }();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
     GemmArgs args = p.args;
     void* params[] = {&args};
     FfmaTmaParams tp;

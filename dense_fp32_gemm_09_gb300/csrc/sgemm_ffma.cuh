@@ -412,6 +412,11 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const Ge
     ld.seek(w, 0);
     Cursor cp = ld;
 
+    // Launched as a programmatic dependent of the stream's previous kernel: the
+    // set-up above overlaps that kernel's tail, and nothing in global memory is
+    // read or written before it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // Prologue: fill STAGES-1 slices.
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {

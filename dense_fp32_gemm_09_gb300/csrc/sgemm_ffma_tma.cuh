@@ -146,6 +146,9 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB)
         }
         abort_s = 0;
         async::mbar_fence_init();
+        // Programmatic dependent launch: the first global read waits for the
+        // stream's previous kernel to complete.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         Cursor ld;   // next slice to load; ld.c = slices issued so far
         ld.seek(s_w, 0);
         for (int s = 0; s < STAGES && ld.c < s_w.total; ++s) {
@@ -158,6 +161,7 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB)
         s_ld = ld;
     }
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // (returns at once by now)
     const CtaWork& w = s_w;
     if (w.total <= 0) return;
     volatile int* abort_flag = &abort_s;
