@@ -45,8 +45,8 @@ __host__ __device__ __forceinline__ long long sk_real_at(long long v, int KT, in
 }
 
 // The gap > 0 forms of the two lookups below, kept out of line: 64-bit
-// divisions are long instruction sequences on the GPU, and the kernels' prologue
-// (fetched cold after an L2 flush) should carry only the equal split's one.
+// divisions are long instruction sequences on the GPU, and with gap 0 the
+// kernels' prologue then carries only the equal split's one.
 inline __host__ __device__ __noinline__ long long sk_begin_gap(const GemmArgs& a, int g) {
     return sk_real_at(sk_virtual_total(a) * g / a.grid, a.KT, a.sk_gap);
 }
