@@ -45,12 +45,26 @@ def describe(w) -> str:
 KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_args.h", "sgemm_epilogue.cuh"]
 
 
-def kernel_sources_hash() -> str:
+def code_only(text: str) -> str:
+    """C++ source text without its comments and with blank space collapsed: what the
+    compiler sees, so that editing a comment does not void a recorded capture."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_sources_hash(read=None) -> str:
+    """sha256 (first 16 hex digits) of the code of KERNEL_SOURCES.  `read(name)`
+    returns a file's text (default: the working tree)."""
     import hashlib
+    if read is None:
+        def read(name):
+            with open(os.path.join(REPO, "dense_fp32_gemm_09_gb300", "csrc", name)) as fh:
+                return fh.read()
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(REPO, "dense_fp32_gemm_09_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        h.update(code_only(read(f)).encode())
     return h.hexdigest()[:16]
 
 
