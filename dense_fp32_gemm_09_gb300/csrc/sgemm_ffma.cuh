@@ -180,7 +180,8 @@ struct Acc<TM, TN, true, BOUTER> {
 // The kernel
 // ----------------------------------------------------------------------------
 template <int BM_, int BN_, int BK_, int TM_, int TN_, int LR_, int WARPS_M_, int WARPS_N_,
-          int STAGES_, int VEC_, int AK_, bool FMA2_, int MINB_, bool PIPE_ = false>
+          int STAGES_, int VEC_, int AK_, bool FMA2_, int MINB_, bool PIPE_ = false,
+          int KU_ = 0>
 struct FfmaCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, TM = TM_, TN = TN_;
     static constexpr int LR = LR_, LC = 32 / LR_;
@@ -193,6 +194,8 @@ struct FfmaCfg {
     // PIPE: load the next k's fragments before the current k's FMAs (register
     // double buffering of A and B fragments inside a slice).
     static constexpr bool PIPE = PIPE_;
+    // KU: AK-deep steps per copy of the unrolled slice loop (0: the whole slice).
+    static constexpr int KU = KU_ > 0 ? KU_ : BK_ / AK_;
     // A slice: [BM][BK + PADA] (row stride odd in 16-byte units); B slice: [BK][BN].
     static constexpr int PADA = ((BK / 4) % 2 == 0) ? 4 : 0;
     static constexpr int LDAS = BK + PADA;
@@ -329,7 +332,7 @@ __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, 
             }
         }
     } else {
-#pragma unroll
+#pragma unroll Cfg::KU
         for (int kq = 0; kq < BK; kq += AK) {
             float av[TM][AK];
             load_a_frag<Cfg>(sA, a_row0, kq, av);
