@@ -260,6 +260,47 @@ def test_stream_k_gap_parity(cuda, oracle_mod, monkeypatch, gap):
     assert used > 0
 
 
+def test_chained_products_see_their_inputs_complete(cuda, oracle_mod):
+    """Back-to-back products on one stream, each reading the one before (the main
+    kernels start as programmatic dependents of the previous kernel, and wait for it
+    before touching memory).  The chain runs a stream-K product whose reduction writes
+    the next one's A, a product whose B is first packed (odd ld, large), and a scaled
+    product that reads C.  Each stage matches the oracle applied to the final value of
+    its inputs."""
+    torch = cuda
+    g = torch.Generator().manual_seed(21)
+
+    def u(r, c, scale):
+        return ((torch.rand(r, c, generator=g) - 0.5) * scale).cuda()
+
+    X0, B1, B2 = u(1100, 1000, 1.0), u(1000, 1024, 0.1), u(1024, 1024, 0.1)
+    B3 = u(1024, 2047, 0.1)            # ld 2047: packed before the product (M*N*K > 2^31)
+    B4, C4 = u(2047, 512, 0.1), u(1100, 512, 1.0)
+    C4_init = C4.clone()
+    C1 = sgemm(X0, B1)
+    C2 = sgemm(C1, B2)
+    C3 = sgemm(C2, B3)
+    sgemm(C3, B4, out=C4, alpha=0.5, beta=2.0)
+    torch.cuda.synchronize()
+    assert sgemm_query_config(1100, 2047, 1024, 1024, 2047, 2047, C2.data_ptr(),
+                              B3.data_ptr(), C3.data_ptr())["packed"] == 2
+
+    def check(A, B, C, alpha=1.0, beta=0.0, C0=None):
+        a, b = A.cpu(), B.cpu()
+        ref = alpha * oracle_mod.gemm_f64(a.numpy(), b.numpy())
+        if C0 is not None:
+            ref = ref + beta * C0.cpu().numpy().astype(np.float64)
+        err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+        tol = abs(alpha) * tolerance(a, b) + (1e-6 * abs(beta) * float(C0.abs().max())
+                                              if C0 is not None else 0.0)
+        assert err <= tol, (tuple(A.shape), tuple(B.shape), err, tol)
+
+    check(X0, B1, C1)
+    check(C1, B2, C2)
+    check(C2, B3, C3)
+    check(C3, B4, C4, 0.5, 2.0, C4_init)
+
+
 def test_caller_workspace_entry_point(cuda, oracle_mod):
     torch = cuda
     from dense_fp32_gemm_09_gb300 import check, sgemm_run_ws, sgemm_workspace_size
