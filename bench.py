@@ -418,7 +418,10 @@ TF32_PER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor rates of the GB3
 
 
 def bench_tf32x3(args, w, dist_ctx):
-    """The 3xTF32 tensor-core variant: one step = operand split + tcgen05 GEMM."""
+    """The 3xTF32 tensor-core variant: one step = one sgemm_tf32x3_run_ex call
+    (operand split + tcgen05 GEMM), inputs resident.  The split and the GEMM are
+    also timed apart through the two-step entry points (whose split writes Ahi too,
+    as the two-step contract needs); the one-call split is the step less the GEMM."""
     import ctypes as ct
 
     import torch
@@ -455,25 +458,41 @@ def bench_tf32x3(args, w, dist_ctx):
         check(lib.sgemm_tf32x3_multiply(*mult), "multiply")
     barrier()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        check(lib.sgemm_tf32x3_prepare(*prep), "prepare")
+        ev[i][1].record(stream)
+        check(lib.sgemm_tf32x3_multiply(*mult), "multiply")
+        ev[i][2].record(stream)
+    barrier()
+    split_full_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    gemm_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+
+    # the timed steps: one public call each, inputs resident
+    run_dev = (w.M, w.N, w.K, args.alpha, dA.data_ptr(), w.K, dB.data_ptr(), w.N, args.beta,
+               dC.data_ptr(), w.N, ws.data_ptr(), need.value, sh)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        check(lib.sgemm_tf32x3_run_ex(*run_dev), "run_ex")
+    barrier()
+    ev1 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     n0 = lib.sgemm_launch_count()
     with ClockSampler(local) as clocks:
         barrier()
         for i in range(args.steps):
             flush.fill_(float(i))
-            ev[i][0].record(stream)
-            check(lib.sgemm_tf32x3_prepare(*prep), "prepare")
-            ev[i][1].record(stream)
-            check(lib.sgemm_tf32x3_multiply(*mult), "multiply")
-            ev[i][2].record(stream)
+            ev1[i][0].record(stream)
+            check(lib.sgemm_tf32x3_run_ex(*run_dev), "run_ex")
+            ev1[i][1].record(stream)
         barrier()
     launches = lib.sgemm_launch_count() - n0
     check(lib.sgemm_device_status(), "device status")
     tcfg = sg.SgemmConfig()
     check(lib.sgemm_tf32x3_query_config(w.M, w.N, w.K, ct.byref(tcfg)), "tf32x3 query")
-    step_ms = statistics.median(e[0].elapsed_time(e[2]) for e in ev)
-    split_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
-    gemm_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    step_ms, split_ms, gemm_ms = max_over_ranks([step_ms, split_ms, gemm_ms], dev)
+    step_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev1)
+    step_ms, split_full_ms, gemm_ms = max_over_ranks([step_ms, split_full_ms, gemm_ms], dev)
+    split_ms = max(step_ms - gemm_ms, 0.0)
 
     # end to end: pinned host in, pinned host out, through the public entry point
     hA, hB = A.pin_memory(), B.pin_memory()
@@ -502,6 +521,7 @@ def bench_tf32x3(args, w, dist_ctx):
         "metric": METRIC, "path": "tf32x3", "value": whole_job_tflops(world, flops, step_ms),
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_ms, "ms_split": split_ms, "ms_gemm": gemm_ms,
+        "ms_split_two_step": split_full_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32x3",
         "data": "synthetic",
         "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,

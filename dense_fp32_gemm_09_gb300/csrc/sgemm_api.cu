@@ -880,11 +880,17 @@ int sgemm_tf32x3_run_ex(int M, int N, int K, float alpha, const float* A, int ld
         return SGEMM_ERR_WORKSPACE;
     }
     const int c_vec = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
-    rc = tf32x3_prepare(M, N, K, A, lda, B, ldb, ws, ws_bytes, d->sms, s);
+    // A that TMA can read (16-byte aligned rows) serves as its own hi part, so the
+    // split writes only Alo for it.  SGEMM_TF32X3_SPLIT_A=1 writes Ahi anyway.
+    const char* split_env = std::getenv("SGEMM_TF32X3_SPLIT_A");
+    const bool force_split = split_env != nullptr && std::atoi(split_env) != 0;
+    const bool a_direct = !force_split && aligned16(A) && lda % 4 == 0;
+    rc = tf32x3_prepare(M, N, K, A, lda, B, ldb, ws, ws_bytes, d->sms, s, !a_direct);
     g_launches.fetch_add(1, std::memory_order_relaxed);   // split_kernel
     if (rc != SGEMM_OK) return rc;
     int n = 0;
-    rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, ws, ws_bytes, d->sms, s, &n);
+    rc = tf32x3_multiply(M, N, K, alpha, beta, C, ldc, c_vec, ws, ws_bytes, d->sms, s, &n,
+                         a_direct ? A : nullptr, lda);
     g_launches.fetch_add(n, std::memory_order_relaxed);
     return rc;
 }

@@ -37,11 +37,14 @@ void shutdown_host_pipes();
 
 // 3xTF32 tensor-core path (sgemm_tf32x3.cu).
 size_t tf32x3_workspace_bytes(int M, int N, int K);
+// write_ahi = false leaves the Ahi region unwritten: the multiply then takes hi
+// from A itself (a_hi = A, lda_hi = lda; A 16-byte aligned with lda % 4 == 0).
 int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const float* B,
-                   long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream);
+                   long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream,
+                   bool write_ahi = true);
 int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
                     int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream,
-                    int* launches);
+                    int* launches, const float* a_hi = nullptr, long long lda_hi = 0);
 int tf32x3_tile_width(int M, int N, int K, int sms);
 int tf32x3_query(int M, int N, int K, int sms, sgemm_config* out);
 

@@ -429,7 +429,8 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 
 // Ahi/Alo[i*Kp + k] for i < M, k < Kp (zeros for K <= k < Kp): chunk e of the
 // M x Kp/4 float4 chunks is row e / (Kp/4), k = 4 (e % (Kp/4)).  Each chunk is
-// read as one float4 when A's row is 16-byte aligned (vec_in) and whole.
+// read as one float4 when A's row is 16-byte aligned (vec_in) and whole.  hi may
+// be null: the GEMM then reads hi straight from A (see below).
 __device__ __forceinline__ void split_a_chunk(const float* __restrict__ A, long long lda, int K,
                                               int Kp, int vec_in, long long e,
                                               float* __restrict__ hi, float* __restrict__ lo) {
@@ -449,7 +450,7 @@ __device__ __forceinline__ void split_a_chunk(const float* __restrict__ A, long 
 #pragma unroll
     for (int u = 0; u < 4; ++u) split_tf32(x[u], h[u], l[u]);
     const long long o = i * Kp + k;
-    *reinterpret_cast<float4*>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
+    if (hi != nullptr) *reinterpret_cast<float4*>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<float4*>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
 }
 
@@ -668,7 +669,8 @@ WsLayout ws_layout(void* ws, int M, int N, int Kp) {
 }  // namespace
 
 int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const float* B,
-                   long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream) {
+                   long long ldb, void* ws, size_t ws_bytes, int sms, cudaStream_t stream,
+                   bool write_ahi) {
     using namespace tc;
     if (ws == nullptr || ws_bytes < tf32x3_workspace_bytes(M, N, K)) {
         set_last_error_message("tf32x3: workspace too small");
@@ -688,8 +690,8 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
     const long long b_blocks = std::min(b_tiles, cap);
     (void)sms;
     split_kernel<<<static_cast<unsigned>(a_blocks + b_blocks), 256, 0, stream>>>(
-        A, lda, M, B, ldb, N, K, Kp, a_vec, b_vec, static_cast<int>(a_blocks), L.ahi, L.alo,
-        L.bhi, L.blo);
+        A, lda, M, B, ldb, N, K, Kp, a_vec, b_vec, static_cast<int>(a_blocks),
+        write_ahi ? L.ahi : nullptr, L.alo, L.bhi, L.blo);
     if (cudaGetLastError() != cudaSuccess) {
         set_last_error_message("tf32x3: split kernels failed to launch");
         return SGEMM_ERR_LAUNCH;
@@ -701,8 +703,9 @@ namespace {
 
 template <int BN>
 int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
-                   int c_vec, const WsLayout& L, size_t partial_bytes, int Kp, int sms,
-                   int schedule, cudaStream_t stream, int* launches) {
+                   int c_vec, const WsLayout& L, const float* a_hi, long long lda_hi,
+                   size_t partial_bytes, int Kp, int sms, int schedule, cudaStream_t stream,
+                   int* launches) {
     using namespace tc;
     using V = Variant<BN>;
     static std::once_flag attr_once;
@@ -717,7 +720,12 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
         return SGEMM_ERR_LAUNCH;
     }
     Params p{};
-    if (!encode_kmajor(&p.tm_ahi, L.ahi, M, K, Kp, V::kBK, BM) ||
+    // The Ahi operand is A itself when the caller's A can be read by TMA: the
+    // tensor core reads an fp32 operand as TF32 by dropping its 13 low mantissa
+    // bits, which is exactly hi (measured bit for bit against the split's hi).
+    const bool direct = a_hi != nullptr;
+    if (!encode_kmajor(&p.tm_ahi, direct ? a_hi : L.ahi, M, K, direct ? lda_hi : Kp, V::kBK,
+                       BM) ||
         !encode_kmajor(&p.tm_alo, L.alo, M, K, Kp, V::kBK, BM) ||
         !encode_kmajor(&p.tm_bhi, L.bhi, N, K, Kp, V::kBK, BN) ||
         !encode_kmajor(&p.tm_blo, L.blo, N, K, Kp, V::kBK, BN)) {
@@ -791,7 +799,7 @@ int tf32x3_query(int M, int N, int K, int sms, sgemm_config* out) {
 
 int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
                     int c_vec, void* ws, size_t ws_bytes, int sms, cudaStream_t stream,
-                    int* launches) {
+                    int* launches, const float* a_hi, long long lda_hi) {
     *launches = 0;
     const size_t need = tf32x3_workspace_bytes(M, N, K);
     if (ws == nullptr || ws_bytes < need) {
@@ -805,10 +813,10 @@ int tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C, long
                                        static_cast<char*>(ws));
     const TcChoice c = tf32x3_choice(M, N, K, sms);
     if (c.bn == 256)
-        return launch_variant<256>(M, N, K, alpha, beta, C, ldc, c_vec, L, partial_bytes, Kp,
-                                   sms, c.schedule, stream, launches);
-    return launch_variant<128>(M, N, K, alpha, beta, C, ldc, c_vec, L, partial_bytes, Kp, sms,
-                               c.schedule, stream, launches);
+        return launch_variant<256>(M, N, K, alpha, beta, C, ldc, c_vec, L, a_hi, lda_hi,
+                                   partial_bytes, Kp, sms, c.schedule, stream, launches);
+    return launch_variant<128>(M, N, K, alpha, beta, C, ldc, c_vec, L, a_hi, lda_hi,
+                               partial_bytes, Kp, sms, c.schedule, stream, launches);
 }
 
 }  // namespace sgemm

@@ -216,7 +216,11 @@ SGEMM_API int sgemm_run_host(int M, int N, int K, const float* hA, int lda, cons
  * per-stream workspace (allocated on first use).  The workspace also holds the
  * partial tiles when the schedule splits tiles between CTAs.  Launches the
  * operand split, the GEMM and, for split tiles, a deterministic reduction.  Any
- * alignment of A, B, C and any leading dimensions.
+ * alignment of A, B, C and any leading dimensions.  When A's rows are 16-byte
+ * aligned (A 16-byte aligned, lda % 4 == 0) the GEMM reads A itself as the hi
+ * part (the tensor core reads fp32 as TF32 by dropping the 13 low mantissa bits,
+ * which is the split's hi) and the split writes only the lo part of A; the
+ * results are the same bit for bit.  SGEMM_TF32X3_SPLIT_A=1 writes both parts.
  * Bounded device-side waits that give up set a flag read by sgemm_device_status(). */
 SGEMM_API int sgemm_tf32x3_run(int M, int N, int K, const float* A, int lda, const float* B,
                                int ldb, float* C, int ldc, sgemm_stream_t stream);

@@ -158,3 +158,27 @@ def test_stream_k_scaled_into_split_tiles(cuda, oracle_mod, monkeypatch):
     ref = oracle_mod.gemm_f64_ex(0.5, A.numpy(), B.numpy(), -1.25, C0.numpy())
     err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
     assert err <= 0.5 * tol(A, B) + 1e-5 * 1.25 * float(C0.abs().max())
+
+
+@pytest.mark.parametrize("M,N,K,lda_pad", [(512, 512, 512, 0), (1000, 700, 1999, 1),
+                                           (3001, 2047, 1999, 5), (129, 300, 33, 3),
+                                           (2048, 64, 4096, 0), (1024, 1024, 1024, 4)])
+def test_hi_read_in_place_is_bit_identical(cuda, tile_width, monkeypatch, M, N, K, lda_pad):
+    """When TMA can read A (16-byte aligned rows), the one-call path feeds A itself as
+    the hi operand instead of writing Ahi: the tensor core reads an fp32 operand as
+    TF32 by dropping its 13 low mantissa bits, which is the split's hi.  The product
+    must equal, bit for bit, the one with Ahi written (SGEMM_TF32X3_SPLIT_A=1),
+    with padded leading dimensions, K not a multiple of 4 and alpha/beta."""
+    torch = cuda
+    A, B = random_pair(M, N, K, seed=M + N + K)
+    lda = K + lda_pad
+    lda += (-lda) % 4                      # 16-byte rows: the in-place path applies
+    buf = torch.full((M, lda), float("nan"), device="cuda")
+    buf[:, :K] = A.cuda()
+    dA, dB = buf[:, :K], B.cuda()
+    C0 = torch.randn(M, N, device="cuda")
+    monkeypatch.delenv("SGEMM_TF32X3_SPLIT_A", raising=False)
+    direct = run(torch, dA, dB, C0.clone(), alpha=0.75, beta=0.5, lda=lda)
+    monkeypatch.setenv("SGEMM_TF32X3_SPLIT_A", "1")
+    split = run(torch, dA, dB, C0.clone(), alpha=0.75, beta=0.5, lda=lda)
+    assert torch.equal(direct, split)
