@@ -217,8 +217,15 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
         name = "256x128x64_t8x16_s2_f2_v4";
     else if (tiles128 * 4 < d.sms)
         name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
-    else if (v4)
-        name = K >= 2048 ? "256x128x64_t8x16_s2_f2_v4" : "256x128x32_t8x16_s4_f2_v4";
+    else if (v4) {
+        // 64-deep slices run about 3% faster; 32-deep ones share K out more finely
+        // over the stream-K ranges.  The deeper ones win once every CTA gets about
+        // 20 of them (measured from 1536^3, where they lose, to 4096x4096x1536).
+        const long long slices64 =
+            static_cast<long long>((M + 255) / 256) * ((N + 127) / 128) * ((K + 63) / 64);
+        name = (K >= 2048 || slices64 >= 20LL * d.sms) ? "256x128x64_t8x16_s2_f2_v4"
+                                                       : "256x128x32_t8x16_s4_f2_v4";
+    }
     else
         name = "128x256x32_t8x16_s3_f2_v1";
     return find_entry(name);
