@@ -13,6 +13,7 @@ using Tall512K32 = FfmaCfg<512, 64, 32, 8, 16, 8, 8, 1, 2, 4, 4, true, 1>;
 using Small8x8 = FfmaCfg<64, 64, 16, 8, 8, 4, 2, 1, 3, 4, 4, true, 4>;
 using Small4x4 = FfmaCfg<64, 64, 16, 4, 4, 4, 4, 2, 3, 4, 4, false, 3>;
 using Small8x4 = FfmaCfg<64, 64, 16, 8, 4, 4, 2, 2, 3, 4, 4, true, 4>;
+using Tiny4x4 = FfmaCfg<32, 32, 16, 4, 4, 4, 2, 1, 3, 4, 4, true, 8>;
 
 static const KernelEntry kEntries[] = {
     make_entry<Tall16x8>("128x64x16_t16x8_s4_f2_v4"),
@@ -20,6 +21,7 @@ static const KernelEntry kEntries[] = {
     make_entry<Small8x8>("64x64x16_t8x8_s3_f2_v4"),
     make_entry<Small4x4>("64x64x16_t4x4_s3_f1_v4"),
     make_entry<Small8x4>("64x64x16_t8x4_s3_f2_v4"),
+    make_entry<Tiny4x4>("32x32x16_t4x4_s3_f2_v4"),
 };
 
 const KernelEntry* ffma_entries_small(int* count) {
