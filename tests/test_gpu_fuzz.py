@@ -95,3 +95,52 @@ def test_random_tf32x3_cases(cuda, oracle_mod, seed):
     for r in range(M):
         mask[offs[2] + r * ldc: offs[2] + r * ldc + N] = False
     assert np.all(flat[mask] == CANARY)
+
+
+def wide_case(rng):
+    """Large shapes drawn around the tile chooser's boundaries: narrow C with M >= 4096
+    (512 x 64 tiles), 64 < N <= 128, K around 2048 (slice depth), the smallest problems
+    (32 x 32 tiles), long K, and short K.  Operands 16-byte aligned."""
+    kind = int(rng.integers(0, 6))
+    lo_hi = [((4000, 4600), (1, 65), (1, 2500)), ((4000, 4600), (65, 129), (1, 1500)),
+             ((1000, 2600), (1000, 2600), (900, 2100)), ((1, 400), (1, 400), (1, 1100)),
+             ((500, 1400), (500, 1400), (1, 4000)), ((1, 2500), (1, 2500), (1, 64))][kind]
+    M, N, K = (int(rng.integers(a, b)) for a, b in lo_hi)
+    return M, N, K
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_wide_cases(cuda, oracle_mod, monkeypatch, seed):
+    """Wide random cases on 16-byte-aligned operands (the 16-byte entries), with random
+    alpha/beta and stream-K gaps forced to 0..3 or left to the planner."""
+    torch = cuda
+    rng = np.random.default_rng(3000 + seed)
+    M, N, K = wide_case(rng)
+    alpha = float(rng.choice([1.0, -1.5, 0.25]))
+    beta = float(rng.choice([0.0, 1.0, -0.5]))
+    gap = str(rng.choice(["", "0", "1", "2", "3"]))
+    if gap:
+        monkeypatch.setenv("SGEMM_SK_GAP", gap)
+    else:
+        monkeypatch.delenv("SGEMM_SK_GAP", raising=False)
+    pads = [(-d) % 4 + 4 * int(rng.integers(0, 2)) for d in (K, N, N)]
+    g = torch.Generator().manual_seed(3000 + seed)
+    A = torch.rand(M, K, generator=g) * 2 - 1
+    B = torch.rand(K, N, generator=g) * 2 - 1
+    C0 = torch.rand(M, N, generator=g) * 2 - 1
+    _, dA, lda = place(torch, A, pads[0], 0, float("nan"))
+    _, dB, ldb = place(torch, B, pads[1], 0, float("nan"))
+    cbuf, dC, ldc = place(torch, C0, pads[2], 0, CANARY)
+    st = sgemm_run_op(0, 0, M, N, K, alpha, dA.data_ptr(), lda, dB.data_ptr(), ldb, beta,
+                      dC.data_ptr(), ldc)
+    assert st == 0, (M, N, K, load().sgemm_last_error())
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm_f64_ex(alpha, A.numpy(), B.numpy(), beta, C0.numpy())
+    err = np.max(np.abs(dC.cpu().numpy().astype(np.float64) - ref))
+    tol = 1e-6 * (abs(alpha) * K + abs(beta)) + 1e-30
+    assert err <= tol, ((M, N, K, alpha, beta, gap), err, tol)
+    flat = cbuf.cpu().numpy()
+    mask = np.ones(flat.size, dtype=bool)
+    for r in range(M):
+        mask[r * ldc: r * ldc + N] = False
+    assert np.all(flat[mask] == CANARY)
