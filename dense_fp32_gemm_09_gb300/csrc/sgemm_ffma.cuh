@@ -147,7 +147,9 @@ struct Acc<TM, TN, true, BOUTER> {
     // B outer with B as the first multiplicand measured 1-3 % faster on the 8x16
     // tile of the cp.async kernels; it keeps all TM broadcast pairs live, which
     // the TMA kernel (A fragments for two k at once) cannot afford, so that one
-    // takes A outer.
+    // takes A outer.  The rows run down for even column pairs and back up for odd
+    // ones, so the FFMA2s on either side of each turn share their A pair: 1.9 %
+    // faster at 4096^3 and 4 % at 1024^3 than restarting every column pair at row 0.
     __device__ __forceinline__ void rank1(const float (&a)[TM], const float4 (&b)[TN / 4]) {
         unsigned long long bp[TN / 2];
 #pragma unroll
@@ -162,7 +164,10 @@ struct Acc<TM, TN, true, BOUTER> {
 #pragma unroll
             for (int j = 0; j < TN / 2; ++j)
 #pragma unroll
-                for (int i = 0; i < TM; ++i) ffma2(v[i][j], bp[j], ap[i]);
+                for (int ii = 0; ii < TM; ++ii) {
+                    const int i = (j & 1) ? TM - 1 - ii : ii;
+                    ffma2(v[i][j], bp[j], ap[i]);
+                }
         } else {
 #pragma unroll
             for (int i = 0; i < TM; ++i)
