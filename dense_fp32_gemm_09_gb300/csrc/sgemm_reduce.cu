@@ -7,6 +7,9 @@
 // CTA order, i.e. in increasing k, which fixes the summation order: the result
 // does not depend on timing.  The schedule formulas are the ones the main
 // kernel used (sgemm_sched.cuh).
+#include <mutex>
+#include <vector>
+
 #include "sgemm_epilogue.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_sched.cuh"
@@ -82,10 +85,22 @@ int reduce_chunks(int bm, int bn, int sk_tiles, int sms) {
 
 cudaError_t launch_sk_reduce(const GemmArgs& a, int bm, int bn, int sms, cudaStream_t stream) {
     // Same shared-memory carveout preference as the GEMM kernels, so the SMs need
-    // not be reconfigured between the two launches.
-    static const cudaError_t carveout = cudaFuncSetAttribute(
-        sk_reduce_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    (void)carveout;
+    // not be reconfigured between the two launches.  It is an attribute of the
+    // kernel in each device's context, so it is set once per device.
+    {
+        static std::mutex mu;
+        static std::vector<char> done;
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) {
+            std::lock_guard<std::mutex> lk(mu);
+            if (static_cast<int>(done.size()) <= dev) done.resize(dev + 1, 0);
+            if (!done[dev]) {
+                (void)cudaFuncSetAttribute(sk_reduce_kernel,
+                                           cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+                done[dev] = 1;
+            }
+        }
+    }
     int chunks = reduce_chunks(bm, bn, a.sk_tiles, sms);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(a.sk_tiles) * chunks);

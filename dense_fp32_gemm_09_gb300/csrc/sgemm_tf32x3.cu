@@ -36,6 +36,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "sgemm_async.cuh"
 #include "sgemm_epilogue.cuh"
@@ -708,16 +709,27 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
                    int* launches) {
     using namespace tc;
     using V = Variant<BN>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(tf32x3_kernel<BN, V::kBK, V::kStages>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(V::kSmem));
-    });
-    if (attr_err != cudaSuccess) {
-        set_last_error_message("tf32x3: cannot set the kernel's shared-memory size");
-        return SGEMM_ERR_LAUNCH;
+    // The shared-memory limit is an attribute of the kernel in each device's
+    // context: raise it once per device this process launches on.
+    static std::mutex attr_mu;
+    static std::vector<int> attr_done;   // per device: 0 not yet, 1 done
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) {
+            set_last_error_message("tf32x3: cudaGetDevice failed");
+            return SGEMM_ERR_LAUNCH;
+        }
+        std::lock_guard<std::mutex> lk(attr_mu);
+        if (static_cast<int>(attr_done.size()) <= dev) attr_done.resize(dev + 1, 0);
+        if (!attr_done[dev]) {
+            if (cudaFuncSetAttribute(tf32x3_kernel<BN, V::kBK, V::kStages>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(V::kSmem)) != cudaSuccess) {
+                set_last_error_message("tf32x3: cannot set the kernel's shared-memory size");
+                return SGEMM_ERR_LAUNCH;
+            }
+            attr_done[dev] = 1;
+        }
     }
     Params p{};
     // The Ahi operand is A itself when the caller's A can be read by TMA: the
