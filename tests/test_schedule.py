@@ -169,3 +169,31 @@ def test_gap_takes_a_store_off_the_1024_cube_critical_path(lib, monkeypatch):
     c0 = _brute_force_critical_path(32, 32, 152, 0, 0, store)
     c1 = _brute_force_critical_path(32, 32, 152, 1, 0, store)
     assert c0 == pytest.approx(7 + 2 * store) and c1 == pytest.approx(7 + store)
+
+
+def test_gap_memo_is_order_independent(lib, monkeypatch):
+    """The planner memoises the gap search per thread (16 slots, hashed by the
+    schedule's numbers).  Interleaving many schedules, in two orders and with forced
+    gaps in between, must give the same gaps as computing each one alone."""
+    monkeypatch.delenv("SGEMM_SK_GAP", raising=False)
+    n = lib.sgemm_num_kernels()
+    cases = [(kid, M, N, K, sms, occ)
+             for kid in range(n)
+             for (M, N, K) in [(1024, 1024, 1024), (3001, 2047, 1999), (4096, 4096, 4096),
+                               (700, 900, 2500), (16384, 64, 4096), (5000, 300, 33)]
+             for (sms, occ) in [(152, 1), (148, 2), (13, 4)]]
+
+    def gaps(order):
+        out = {}
+        for c in order:
+            cfg = _cfg()
+            assert lib.sgemm_schedule_check(*c, 0, ctypes.byref(cfg)) == 0
+            out[c] = cfg.sk_gap
+        return out
+
+    first = gaps(cases)
+    monkeypatch.setenv("SGEMM_SK_GAP", "2")
+    gaps(cases[::3])
+    monkeypatch.delenv("SGEMM_SK_GAP")
+    assert gaps(cases[::-1]) == first
+    assert any(g > 0 for g in first.values()) and any(g == 0 for g in first.values())
