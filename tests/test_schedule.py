@@ -186,8 +186,9 @@ def test_gap_memo_is_order_independent(lib, monkeypatch):
     def gaps(order):
         out = {}
         for c in order:
+            kid, M, N, K, sms, occ = c
             cfg = _cfg()
-            assert lib.sgemm_schedule_check(*c, 0, ctypes.byref(cfg)) == 0
+            assert lib.sgemm_schedule_check(M, N, K, kid, sms, occ, 0, ctypes.byref(cfg)) == 0
             out[c] = cfg.sk_gap
         return out
 
