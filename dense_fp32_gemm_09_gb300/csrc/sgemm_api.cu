@@ -199,21 +199,15 @@ bool entry_fits(const KernelEntry& e, const float* A, int lda, const float* B, i
     return e.vec != 4 || vec4_ok(A, lda, B, ldb);
 }
 
-int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int lda,
-                 const float* B, int ldb) {
-    if (const char* force = std::getenv("SGEMM_FORCE_KERNEL")) {
-        const int id = find_entry(force);
-        if (id >= 0 && entry_fits(table()[id], A, lda, B, ldb) && d.occ[id] > 0)
-            return id;
-    }
-    const bool v4 = vec4_ok(A, lda, B, ldb);
+// The per-shape rules on their own: `sms` SMs, `v4` when 16-byte loads serve A and B.
+int choose_by_rules(int sms, int M, int N, int K, bool v4) {
     const long long tiles128 = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
     const long long tiles64 = static_cast<long long>((M + 63) / 64) * ((N + 63) / 64);
     const char* name;
     if (v4 && N <= 64 && M >= 4096)
         // Narrow C: 512-row tiles once M fills 8 of them.
         name = "512x64x32_t8x16_s2_f2_v4";
-    else if (v4 && tiles64 * 4 <= d.sms && K <= 1024)
+    else if (v4 && tiles64 * 4 <= sms && K <= 1024)
         // The smallest problems: 32 x 32 tiles give the SMs four times as many
         // tiles (256^3: 10.9 against 13.0 us; 384^3: 13.0-14.0 against 15.0).
         name = "32x32x16_t4x4_s3_f2_v4";
@@ -222,7 +216,7 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
     else if (v4 && N <= 128 && M >= 4096)
         // A 256-wide tile would compute half its columns for nothing.
         name = "256x128x64_t8x16_s2_f2_v4";
-    else if (tiles128 * 4 < d.sms)
+    else if (tiles128 * 4 < sms)
         name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
     else if (v4) {
         // 64-deep slices run about 3% faster; 32-deep ones share K out more finely
@@ -230,12 +224,22 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
         // 20 of them (measured from 1536^3, where they lose, to 4096x4096x1536).
         const long long slices64 =
             static_cast<long long>((M + 255) / 256) * ((N + 127) / 128) * ((K + 63) / 64);
-        name = (K >= 2048 || slices64 >= 20LL * d.sms) ? "256x128x64_t8x16_s2_f2_v4"
-                                                       : "256x128x32_t8x16_s4_f2_v4";
+        name = (K >= 2048 || slices64 >= 20LL * sms) ? "256x128x64_t8x16_s2_f2_v4"
+                                                     : "256x128x32_t8x16_s4_f2_v4";
     }
     else
         name = "128x256x32_t8x16_s3_f2_v1";
     return find_entry(name);
+}
+
+int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int lda,
+                 const float* B, int ldb) {
+    if (const char* force = std::getenv("SGEMM_FORCE_KERNEL")) {
+        const int id = find_entry(force);
+        if (id >= 0 && entry_fits(table()[id], A, lda, B, ldb) && d.occ[id] > 0)
+            return id;
+    }
+    return choose_by_rules(d.sms, M, N, K, vec4_ok(A, lda, B, ldb));
 }
 
 // Time to store one BM x BN tile, in BK-deep slices of the same tile.  A slice
@@ -854,6 +858,20 @@ int sgemm_schedule_check(int M, int N, int K, int kernel_id, int sms, int ctas_p
     make_schedule(sms, ctas_per_sm, kernel_id, schedule, p);
     if (out) fill_config(p, out);
     return check_schedule(p, t_last_error, sizeof(t_last_error));
+}
+
+int sgemm_choose_check(int M, int N, int K, int lda, int ldb, int a_offset, int b_offset,
+                       int sms, int* kernel_id, int* packed) {
+    if (M <= 0 || N <= 0 || K <= 0 || lda < K || ldb < N || sms <= 0 || a_offset < 0 ||
+        a_offset > 3 || b_offset < 0 || b_offset > 3 || kernel_id == nullptr)
+        return SGEMM_ERR_INVALID_ARG;
+    // Stand-ins that carry only the operands' alignment.
+    const float* pa = reinterpret_cast<const float*>(uintptr_t{256} + 4u * a_offset);
+    const float* pb = reinterpret_cast<const float*>((uintptr_t{256} << 20) + 4u * b_offset);
+    const PackPlan q = pack_plan(M, N, K, pa, lda, pb, ldb, true, -1, 0, 0);
+    *kernel_id = choose_by_rules(sms, M, N, K, vec4_ok(q.plan_a, q.lda, q.plan_b, q.ldb));
+    if (packed) *packed = (q.pack_a ? 1 : 0) | (q.pack_b ? 2 : 0);
+    return *kernel_id >= 0 ? SGEMM_OK : SGEMM_ERR_UNSUPPORTED;
 }
 
 int sgemm_tf32x3_workspace_size(int M, int N, int K, size_t* out_bytes) {

@@ -276,6 +276,18 @@ SGEMM_API int sgemm_selftest_bounded_wait(int limit_ms);
 SGEMM_API int sgemm_schedule_check(int M, int N, int K, int kernel_id, int sms, int ctas_per_sm,
                                    int schedule, sgemm_config* out);
 
+/* Host-only view of the per-shape tile table (no GPU needed): the entry that
+ * sgemm_run picks for an M x N x K product with leading dimensions lda, ldb (in
+ * floats) on a GPU with `sms` SMs.  `a_offset` and `b_offset` (0..3) place the
+ * start of A and B that many floats past a 16-byte boundary.  As in sgemm_run,
+ * a large product with a misaligned operand is planned on its aligned packed
+ * copy; `packed` (may be NULL) receives 1 if A would be packed, 2 if B, 3 for
+ * both.  SGEMM_FORCE_KERNEL is not consulted.  Returns SGEMM_ERR_INVALID_ARG for
+ * M, N or K <= 0, lda < K, ldb < N, sms <= 0, an offset outside 0..3 or a NULL
+ * kernel_id. */
+SGEMM_API int sgemm_choose_check(int M, int N, int K, int lda, int ldb, int a_offset,
+                                 int b_offset, int sms, int* kernel_id, int* packed);
+
 /* Number of entries in the tile table, and entry `kernel_id`'s static shape
  * (grid, tiles, sk_tiles and split_k are left 0). */
 SGEMM_API int sgemm_num_kernels(void);

@@ -1,6 +1,6 @@
 """The boundary as a C user sees it (no GPU): a C99 program and the same source as
 C++17 include include/sgemm.h, link libsgemm_gb300.so and call the entry points
-that need no device (tile table, schedule check, argument rejection)."""
+that need no device (tile table, tile choice, schedule check, argument rejection)."""
 import os
 import shutil
 import subprocess
@@ -20,6 +20,9 @@ int main(void) {
     if (sgemm_schedule_check(1024, 1024, 1024, 0, 152, 1, 0, &c) != SGEMM_OK) return 3;
     if (sgemm_run(-1, 4, 4, 0, 4, 0, 4, 0, 4, 0) != SGEMM_ERR_INVALID_ARG) return 4;
     if (sgemm_kernel_info(n, &c) != SGEMM_ERR_UNSUPPORTED) return 5;
+    int kid = -1, packed = -1;
+    if (sgemm_choose_check(4096, 4096, 4096, 4096, 4096, 0, 0, 152, &kid, &packed) != SGEMM_OK ||
+        kid < 0 || kid >= n || packed != 0) return 6;
     printf("%s %d\n", sgemm_status_string(SGEMM_OK), n);
     return 0;
 }
