@@ -427,8 +427,6 @@ int launch(const Plan& p, cudaStream_t stream) {
     return SGEMM_OK;
 }
 
-// Common body of the run entry points.  ws == nullptr with ws_bytes == SIZE_MAX
-// means "use the library-owned workspace".
 // Row-by-row copy of a rows x cols matrix into a buffer whose leading dimension
 // ldd is a multiple of 4 (16-byte rows), for operands whose own rows are not
 // 16-byte aligned.  Each thread moves 4 consecutive elements of one row.
@@ -561,7 +559,10 @@ PackPlan pack_plan(int M, int N, int K, const float* A, int lda, const float* B,
     return q;
 }
 
-// C = alpha * A.B + beta * C; the plain entry points pass alpha = 1, beta = 0.
+// Common body of the run entry points: C = alpha * op(A).op(B) + beta * C (the
+// plain entry points pass alpha = 1, beta = 0).  library_ws selects the
+// library-owned workspace; otherwise the caller's (ws, ws_bytes) serves the
+// split tiles and nothing is staged.
 int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const float* B, int ldb,
              float beta, float* C, int ldc, int forced_entry, int schedule, void* ws,
              size_t ws_bytes, bool library_ws, cudaStream_t stream, int transa = 0,

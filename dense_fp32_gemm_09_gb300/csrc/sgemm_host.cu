@@ -248,9 +248,19 @@ int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* h
         if (e != cudaSuccess) failed = "device-to-host copy";
     }
     const cudaError_t fail_e = e;
-    // Join: `s` continues once the last panel is back (which orders every
-    // copy and product before it); also on failure, so `s` stays ordered.
-    cudaError_t j = cudaEventRecord(hp->done, hp->d2h);
+    // Join: `s` continues once the last panel is back, which on success follows
+    // every copy and product of this call.  After a failure part of the
+    // pipeline may not lead to that copy (copies in of later panels, say), so
+    // the other two streams are joined as well.  A wait uses the event as last
+    // recorded when the wait is issued, so `done` serves all three.
+    cudaError_t j = cudaSuccess;
+    if (failed != nullptr || rc != SGEMM_OK) {
+        for (cudaStream_t st : {hp->h2d, hp->comp}) {
+            if (j == cudaSuccess) j = cudaEventRecord(hp->done, st);
+            if (j == cudaSuccess) j = cudaStreamWaitEvent(s, hp->done, 0);
+        }
+    }
+    if (j == cudaSuccess) j = cudaEventRecord(hp->done, hp->d2h);
     if (j == cudaSuccess) j = cudaStreamWaitEvent(s, hp->done, 0);
     if (failed != nullptr) {
         set_cuda_error(failed, fail_e);

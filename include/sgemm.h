@@ -150,7 +150,14 @@ SGEMM_API int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const f
 SGEMM_API int sgemm_run_noalloc(int M, int N, int K, const float* A, int lda, const float* B,
                                 int ldb, float* C, int ldc, sgemm_stream_t stream);
 
-/* Bytes of workspace sgemm_run_ws needs for these arguments (0 if none). */
+/* Bytes of workspace sgemm_run_ws needs for these arguments on the current
+ * device (0 if none).  The pointers matter only through their alignment, which
+ * selects the tile-table entry; NULL assumes a 16-byte-aligned operand, so pass
+ * the real pointers when they may be misaligned (sgemm_run_ws rejects a workspace
+ * that turns out too small with SGEMM_ERR_WORKSPACE; it never overruns it).
+ * Returns SGEMM_ERR_INVALID_ARG for a negative size, a leading dimension below
+ * its row width or a NULL out_bytes, and SGEMM_ERR_UNSUPPORTED when the current
+ * device is not an sm_103 GPU. */
 SGEMM_API int sgemm_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
                          const float* A, const float* B, const float* C, size_t* out_bytes);
 
