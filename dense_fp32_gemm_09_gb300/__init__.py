@@ -24,13 +24,36 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
+# The C ABI takes sizes and leading dimensions as 32-bit ints; ctypes would
+# silently wrap a larger Python int, so the binding rejects it instead.
+_INT_MAX = 2**31 - 1
+
+
+def _fits_int(name: str, **values) -> None:
+    for what, v in values.items():
+        if v > _INT_MAX:
+            raise ValueError(f"{name}: {what} = {v} does not fit the library's 32-bit ints")
+
+
+def _stored_ld(step: int, lines: int, width: int, name: str) -> int:
+    """Leading dimension of `lines` stored rows of `width` elements that start
+    `step` elements apart.  Rows that overlap (step < width) would make the
+    library read or write past the view, so they are rejected; a single row has
+    no step to speak of."""
+    if lines > 1 and step < width:
+        raise ValueError(f"{name}: its rows overlap (row stride {step} < row width {width})")
+    ld = max(step, width, 1)
+    _fits_int(name, leading_dimension=ld)
+    return ld
+
+
 def _ld(t, name: str) -> int:
     """Leading dimension of a 2-D row-major tensor view (unit column stride)."""
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D")
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must have unit stride along its columns")
-    return max(t.stride(0), t.shape[1], 1)
+    return _stored_ld(t.stride(0), t.shape[0], t.shape[1], name)
 
 
 def _layout(t, name: str) -> tuple[int, int]:
@@ -40,9 +63,9 @@ def _layout(t, name: str) -> tuple[int, int]:
         raise ValueError(f"{name} must be 2-D")
     rows, cols = t.shape
     if cols <= 1 or t.stride(1) == 1:
-        return 0, max(t.stride(0), cols, 1)
+        return 0, _stored_ld(t.stride(0), rows, cols, name)
     if rows <= 1 or t.stride(0) == 1:
-        return 1, max(t.stride(1), rows, 1)
+        return 1, _stored_ld(t.stride(1), cols, rows, name)
     raise ValueError(f"{name} needs a unit stride along its rows or its columns")
 
 
@@ -158,6 +181,10 @@ def sgemm(A, B, out=None, *, alpha: float = 1.0, beta: float = 0.0,
         _check_operand(out, "out")
         if tuple(out.shape) != (M, N):
             raise ValueError(f"out must be {(M, N)}, got {tuple(out.shape)}")
+    if B.device != A.device or out.device != A.device:
+        raise ValueError(f"A, B and out must be on one device: {A.device}, {B.device}, "
+                         f"{out.device}")
+    _fits_int("sgemm", M=M, N=N, K=K)
     if M == 0 or N == 0:
         return out
     (ta, lda), (tb, ldb), ldc = _layout(A, "A"), _layout(B, "B"), _ld(out, "out")

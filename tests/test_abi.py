@@ -127,3 +127,55 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(_abi, "library_path", lambda: str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         _abi.load()
+
+
+def test_binding_layout_of_views():
+    # Stride logic only (CPU tensors): what leading dimension each view maps to.
+    import torch
+    from dense_fp32_gemm_09_gb300 import _layout, _ld
+    X = torch.zeros(6, 10)
+    assert _layout(X, "X") == (0, 10)
+    assert _layout(X[:, 2:7], "X") == (0, 10)            # column slice keeps the row step
+    assert _layout(X.t(), "X") == (1, 10)                # transpose of a row-major view
+    assert _layout(X[1:2], "X") == (0, 10)               # one row
+    assert _layout(X[:, 3:4], "X") == (0, 10)            # one column
+    assert _layout(torch.zeros(5, 0), "X")[0] == 0       # K = 0
+    assert _ld(X[2:5, 1:9], "out") == 10
+
+
+@pytest.mark.parametrize("make", [
+    lambda t: t.zeros(1).expand(4, 1),                   # every row is the same element
+    lambda t: t.zeros(8).as_strided((3, 4), (2, 1)),     # rows overlap by half
+    lambda t: t.zeros(8).as_strided((4, 3), (1, 2)).t().t(),
+    lambda t: t.zeros(16).as_strided((3, 4), (1, 2)),    # transposed view whose columns overlap
+])
+def test_binding_rejects_overlapping_rows(make):
+    # The library would read (or, for `out`, write) past such a view's storage.
+    import torch
+    from dense_fp32_gemm_09_gb300 import _layout, _ld
+    v = make(torch)
+    with pytest.raises(ValueError, match="overlap"):
+        _layout(v, "A")
+    if v.shape[1] <= 1 or v.stride(1) == 1:
+        with pytest.raises(ValueError, match="overlap"):
+            _ld(v, "out")
+
+
+def test_binding_rejects_values_beyond_32_bits():
+    # ctypes would wrap 2**32 + 5 to 5 without a word.
+    from dense_fp32_gemm_09_gb300 import _fits_int, _layout
+    _fits_int("x", M=2**31 - 1)
+    with pytest.raises(ValueError, match="32-bit"):
+        _fits_int("x", K=2**31)
+
+    class View:   # shape and strides of a view too large to allocate here
+        shape = (2, 3)
+
+        def dim(self):
+            return 2
+
+        def stride(self, i):
+            return (2**31, 1)[i]
+
+    with pytest.raises(ValueError, match="32-bit"):
+        _layout(View(), "A")
