@@ -98,7 +98,9 @@ typedef struct {
  * from the 4-byte-load kernels' in rounding, as any two tilings can, and stay
  * within the same bound).  The first call that needs
  * a workspace must not be made while the stream is being captured into a CUDA
- * graph.  The product kernel is launched as a programmatic dependent of the
+ * graph.  One workspace is kept for every (device, stream handle) that needed
+ * one, until sgemm_shutdown; a program that cycles through many short-lived
+ * streams is better served by sgemm_run_ws or sgemm_run_noalloc.  The product kernel is launched as a programmatic dependent of the
  * stream's previous kernel: its set-up may overlap that kernel's tail, and it
  * waits for that kernel to complete before reading or writing global memory, so
  * stream order holds as for a plain launch (SGEMM_PDL=0 launches it plainly). */
