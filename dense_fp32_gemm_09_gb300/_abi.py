@@ -61,6 +61,7 @@ SIGNATURES = {
     "sgemm_selftest_bounded_wait": (_i, [_i]),
     "sgemm_schedule_check": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(SgemmConfig)]),
     "sgemm_choose_check": (_i, [_i] * 8 + [ctypes.POINTER(_i), ctypes.POINTER(_i)]),
+    "sgemm_host_plan_check": (_i, [_i, _i, _i] + [ctypes.POINTER(_i)] * 3),
     "sgemm_num_kernels": (_i, []),
     "sgemm_kernel_info": (_i, [_i, ctypes.POINTER(SgemmConfig)]),
     "sgemm_kernel_name": (ctypes.c_char_p, [_i]),

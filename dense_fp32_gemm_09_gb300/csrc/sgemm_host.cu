@@ -19,7 +19,7 @@ namespace {
 // copies, the product of each row panel of C, device-to-host copies), so that
 // the copies of one panel overlap the product of another.
 // ----------------------------------------------------------------------------
-constexpr int kMaxHostPanels = 16;
+constexpr int kMaxHostPanels = SGEMM_HOST_MAX_PANELS;
 struct HostPipe {
     int dev = 0;
     cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
@@ -111,13 +111,13 @@ int host_panels(int M, int N, int K, int (&rows)[kMaxHostPanels]) {
             for (int i = 0; i < n_pct; ++i) pct[i] = 1;
         }
     }
-    int total = 0;
+    long long total = 0;
     for (int i = 0; i < n_pct; ++i) total += pct[i];
     int n = 0, done = 0;
     for (int i = 0; i < n_pct && done < M; ++i) {
         // Panels of whole 256-row tiles (two 128-row ones): a panel that ends
         // inside a tile row computes the rest of that row for nothing.
-        int r = static_cast<int>(static_cast<long long>(M) * pct[i] / total);
+        int r = static_cast<int>(M * static_cast<long long>(pct[i]) / total);
         r = std::max(256, (r + 128) / 256 * 256);
         if (i == n_pct - 1 || done + r > M) r = M - done;
         rows[n++] = r;
@@ -161,6 +161,17 @@ void shutdown_host_pipes() {
 using namespace sgemm;
 
 extern "C" {
+
+int sgemm_host_plan_check(int M, int N, int K, int* n_panels, int* rows, int* k_chunk) {
+    if (M <= 0 || N <= 0 || K < 0 || n_panels == nullptr) return SGEMM_ERR_INVALID_ARG;
+    int r[kMaxHostPanels];
+    const int n = host_panels(M, N, K, r);
+    *n_panels = n;
+    if (rows)
+        for (int i = 0; i < n; ++i) rows[i] = r[i];
+    if (k_chunk) *k_chunk = K > 0 ? host_kchunk(M, N, K) : 0;
+    return SGEMM_OK;
+}
 
 int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* hB, int ldb,
                    float* hC, int ldc, float* dA, float* dB, float* dC, sgemm_stream_t stream) {

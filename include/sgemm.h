@@ -96,14 +96,15 @@ typedef struct {
  * so they run on the 16-byte / TMA kernels (the copy moves values, not sums: the
  * results are those of the aligned kernels on aligned operands; they can differ
  * from the 4-byte-load kernels' in rounding, as any two tilings can, and stay
- * within the same bound).  The first call that needs
- * a workspace must not be made while the stream is being captured into a CUDA
- * graph.  One workspace is kept for every (device, stream handle) that needed
- * one, until sgemm_shutdown; a program that cycles through many short-lived
- * streams is better served by sgemm_run_ws or sgemm_run_noalloc.  The product kernel is launched as a programmatic dependent of the
- * stream's previous kernel: its set-up may overlap that kernel's tail, and it
- * waits for that kernel to complete before reading or writing global memory, so
- * stream order holds as for a plain launch (SGEMM_PDL=0 launches it plainly). */
+ * within the same bound).  The first call that needs a workspace must not be
+ * made while the stream is being captured into a CUDA graph.  One workspace is
+ * kept for every (device, stream handle) that needed one, until sgemm_shutdown;
+ * a program that cycles through many short-lived streams is better served by
+ * sgemm_run_ws or sgemm_run_noalloc.  The product kernel is launched as a
+ * programmatic dependent of the stream's previous kernel: its set-up may overlap
+ * that kernel's tail, and it waits for that kernel to complete before reading or
+ * writing global memory, so stream order holds as for a plain launch
+ * (SGEMM_PDL=0 launches it plainly). */
 SGEMM_API int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
               float* C, int ldc, sgemm_stream_t stream);
 
@@ -215,6 +216,19 @@ SGEMM_API int sgemm_run_op(int transa, int transb, int M, int N, int K, float al
 SGEMM_API int sgemm_run_host(int M, int N, int K, const float* hA, int lda, const float* hB, int ldb,
                    float* hC, int ldc, float* dA, float* dB, float* dC,
                    sgemm_stream_t stream);
+
+/* Most row panels (and k-chunks of the first panel) sgemm_run_host splits into. */
+#define SGEMM_HOST_MAX_PANELS 16
+
+/* Host-only view of sgemm_run_host's plan (no GPU needed): the number of row
+ * panels of C in *n_panels, their heights in rows[0 .. *n_panels - 1] (rows may
+ * be NULL; else it holds SGEMM_HOST_MAX_PANELS ints) and the depth of the first
+ * panel's k-chunks in *k_chunk (K when it is not chunked, 0 for K == 0; may be
+ * NULL).  The panels cover M in order, every one but the last a multiple of 256
+ * rows.  The tuning variables SGEMM_HOST_SPLIT, SGEMM_HOST_PANELS and
+ * SGEMM_HOST_KCHUNKS are honoured as in sgemm_run_host.  Returns
+ * SGEMM_ERR_INVALID_ARG for M or N <= 0, K < 0 or a NULL n_panels. */
+SGEMM_API int sgemm_host_plan_check(int M, int N, int K, int* n_panels, int* rows, int* k_chunk);
 
 /* 3xTF32 tensor-core variant (tcgen05, TMEM, TMA): C = alpha * A.B + beta * C with
  * each operand split into two TF32 numbers, x = hi + lo, and
