@@ -219,6 +219,17 @@ def oracle_rate(w, A, B, target_s: float = 12.0, max_rows: int | None = None):
             "seconds": dt}
 
 
+L2_NOTE = ("GPU arm: L2 flushed before every step (256 MiB write, outside the timed "
+           "events); the oracle arm runs on the host cores")
+
+
+def workload_config(w, world: int, extra: str = "") -> dict:
+    """The `config` of a bench line: the workload and how it is run, the same for
+    the GPU arm and the oracle (reference) arm of the same workload."""
+    return {"workload": describe(w) + extra, "M": w.M, "N": w.N, "K": w.K, "l2": L2_NOTE,
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -237,7 +248,7 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * statistics.median(steps_t), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K},
+            "config": workload_config(w, args.gpus),
             "cpu_baseline": {**{k: v for k, v in r.items() if k != "seconds"}, "value": value},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -385,15 +396,13 @@ def bench_line(args, w, world, med_ms, mean_ms, t_wall, e2e_ms, clocks, cfg, lau
         "ms_per_step_mean": mean_ms, "wall_s_timed_region": t_wall,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": describe(w) + (f"; C = {args.alpha:g}*A.B + {args.beta:g}*C"
-                                              if scaled else "")
-                   + (f"; operands {args.trans} (T = stored transposed, transposed on the "
-                      f"device inside the step)" if trans else ""),
-                   "M": w.M, "N": w.N, "K": w.K,
-                   "l2": "flushed before every step (256 MiB write, outside the events)",
-                   "kernel": cfg["name"], "grid": cfg["grid"], "tiles": cfg["tiles"],
-                   "sk_tiles": cfg["sk_tiles"], "ctas_per_sm": cfg["ctas_per_sm"],
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": workload_config(
+            w, world, (f"; C = {args.alpha:g}*A.B + {args.beta:g}*C" if scaled else "")
+            + (f"; operands {args.trans} (T = stored transposed, transposed on the device "
+               f"inside the step)" if trans else "")),
+        "plan": {"kernel": cfg["name"], "grid": cfg["grid"], "tiles": cfg["tiles"],
+                 "sk_tiles": cfg["sk_tiles"], "cluster": cfg["cluster"],
+                 "ctas_per_sm": cfg["ctas_per_sm"]},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops,
                      "unit": "TFLOP/s", "frac": achieved / peak_tflops,
                      "traffic": None if trans else recorded_traffic(cfg["name"], w.name),
@@ -524,12 +533,10 @@ def bench_tf32x3(args, w, dist_ctx):
         "ms_split_two_step": split_full_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32x3",
         "data": "synthetic",
-        "config": {"workload": describe(w), "M": w.M, "N": w.N, "K": w.K,
-                   "l2": "flushed before every step (256 MiB write, outside the events)",
-                   "kernel": f"tf32x3_kernel<BN={tcfg.bn}, {tcfg.stages} stages> + split "
-                             f"kernels" + (" + sk_reduce_kernel" if tcfg.sk_tiles else ""),
-                   "grid": tcfg.grid, "tiles": tcfg.tiles, "sk_tiles": tcfg.sk_tiles,
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": workload_config(w, world),
+        "plan": {"kernel": f"tf32x3_kernel<BN={tcfg.bn}, {tcfg.stages} stages> + split "
+                           f"kernels" + (" + sk_reduce_kernel" if tcfg.sk_tiles else ""),
+                 "grid": tcfg.grid, "tiles": tcfg.tiles, "sk_tiles": tcfg.sk_tiles},
         "roofline": {"bound": "tensor", "achieved": 3 * flops / (gemm_ms * 1e-3) / 1e12,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": 3 * flops / (gemm_ms * 1e-3) / 1e12 / peak, "traffic": None,

@@ -26,7 +26,7 @@ class SgemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "bm", "bn", "bk", "wm", "wn", "tm", "tn", "stages", "threads", "smem_bytes",
         "split_k", "kernel_id", "vec", "grid", "tiles", "sk_tiles", "ctas_per_sm", "fma2",
-        "packed", "sk_gap")]
+        "packed", "sk_gap", "cluster")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -248,17 +248,23 @@ int choose_entry(const DeviceInfo& d, int M, int N, int K, const float* A, int l
 // both shared alike when several CTAs sit on one SM), so the ratio is ~12 / BK.
 double store_cost_slices(const KernelEntry& e) { return 12.0 / e.bk; }
 
-// schedule: 0 automatic, 1 data-parallel only, 2 stream-K whenever possible.
+// schedule: 0 automatic, 1 data-parallel only, 2 stream-K whenever possible,
+// 3 cluster split whenever possible.
 // SGEMM_SK_GAP=<n> asks for that stream-K gap where it is allowed;
-// SGEMM_GROUP_M=<n> sets the raster group height (tuning).
+// SGEMM_GROUP_M=<n> sets the raster group height; SGEMM_CLUSTER=<S> asks for
+// clusters of up to S CTAs per tile where allowed, 0 for none (tuning).
 void make_schedule(int sms, int occ, int entry, int schedule, Plan& p) {
     const KernelEntry& e = table()[entry];
-    int forced_gap = -1, group_m = 0;
+    int forced_gap = -1, group_m = 0, forced_cluster = -1;
     if (const char* g = std::getenv("SGEMM_SK_GAP")) forced_gap = std::atoi(g);
     if (const char* g = std::getenv("SGEMM_GROUP_M")) group_m = std::max(0, std::atoi(g));
+    if (const char* g = std::getenv("SGEMM_CLUSTER")) forced_cluster = std::max(0, std::atoi(g));
+    // The cp.async kernels sum cluster-split tiles in distributed shared memory;
+    // the TMA-fed ones only take the stream-K reduction.
+    const int cluster_max = e.tma ? 0 : kMaxCluster;
     const SchedSizes z = plan_schedule(p.args, e.bm, e.bn, e.bk, sms, occ, schedule,
                                        store_cost_slices(e), forced_gap < 0 ? -1 : forced_gap,
-                                       group_m);
+                                       group_m, cluster_max, forced_cluster);
     p.ctas_per_sm = occ;
     p.split = z.split;
     p.ws_partial_bytes = z.partial_bytes;
@@ -390,11 +396,23 @@ int launch(const Plan& p, cudaStream_t stream) {
         const char* v = std::getenv("SGEMM_PDL");
         return v == nullptr || std::atoi(v) != 0;
     }();
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = pdl ? attr : nullptr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    unsigned nattr = 0;
+    if (pdl) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    if (p.args.cl_split > 1) {
+        // Cluster split: CTAs t*S .. t*S+S-1 (one tile) form one cluster.
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(p.args.cl_split);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+    }
+    cfg.attrs = nattr ? attr : nullptr;
+    cfg.numAttrs = nattr;
     GemmArgs args = p.args;
     void* params[] = {&args};
     FfmaTmaParams tp;
@@ -416,7 +434,7 @@ int launch(const Plan& p, cudaStream_t stream) {
         set_error(e.name, err);
         return SGEMM_ERR_LAUNCH;
     }
-    if (p.args.sk_tiles > 0) {
+    if (p.args.sk_tiles > 0 && p.args.cl_split <= 1) {
         err = launch_sk_reduce(p.args, e.bm, e.bn, p.sms, stream);
         g_launches.fetch_add(1, std::memory_order_relaxed);
         if (err != cudaSuccess) {
@@ -663,6 +681,7 @@ void fill_config(const Plan& p, sgemm_config* out) {
     out->ctas_per_sm = p.ctas_per_sm;
     out->fma2 = e.fma2;
     out->sk_gap = p.args.sk_gap;
+    out->cluster = p.args.cl_split > 1 ? p.args.cl_split : 0;
 }
 
 // Walks every CTA's flat slice list exactly as the kernel does and checks the
@@ -679,6 +698,32 @@ int check_schedule(const Plan& p, char* why, size_t why_len) {
         return SGEMM_ERR_INVALID_ARG;
     };
     if (G <= 0 || a.dp_tiles + a.sk_tiles != T) return fail("tile count", G, T);
+    const int S = a.cl_split;
+    if (S > 1) {
+        // Cluster split: T clusters of S CTAs, CTA t*S+r holds a non-empty piece
+        // of tile t only, pieces in rank order, the cluster size divides BM.
+        if (S > kMaxCluster || (S & (S - 1)) != 0) return fail("cluster size", S, 0);
+        if (a.dp_tiles != 0 || static_cast<long long>(a.sk_tiles) * S != G || a.sk_gap != 0)
+            return fail("cluster grid", G, a.sk_tiles);
+        if (e.bm % S != 0 || e.tma) return fail("cluster sum unsupported", e.bm, S);
+        for (int g = 0; g < G; ++g) {
+            const CtaWork w = make_work(a, g);
+            if (w.total <= 0) return fail("CTA without work", g, w.total);
+            // The kernels' division-free form of the same work.
+            const CtaWork wc = make_cluster_work(a, g);
+            if (wc.u0 != w.u0 || wc.u1 != w.u1 || wc.total != w.total || wc.dp_iters != 0 ||
+                w.dp_iters != 0)
+                return fail("cluster work differs from the stream-K formula", g, wc.u0);
+            Cursor c;
+            c.seek(w, 0);
+            const int want_tile = g / S;
+            if (c.tile != want_tile || c.kt_begin != static_cast<int>(
+                                           static_cast<long long>(KT) * (g % S) / S) ||
+                c.kt_end != static_cast<int>(static_cast<long long>(KT) * (g % S + 1) / S) ||
+                w.total != c.kt_end - c.kt_begin)
+                return fail("cluster piece", g, c.tile);
+        }
+    }
     if (a.sk_tiles > 0 && a.sk_iters < G) return fail("stream-K range empty", a.sk_iters, G);
     if (a.sk_tiles > G) return fail("more split tiles than CTAs", a.sk_tiles, G);
     std::vector<unsigned char> cover(static_cast<size_t>(T) * KT, 0);
@@ -761,7 +806,7 @@ int sgemm_run(int M, int N, int K, const float* A, int lda, const float* B, int 
 int sgemm_run_ex(int M, int N, int K, float alpha, const float* A, int lda, const float* B,
                  int ldb, float beta, float* C, int ldc, int kernel_id, int schedule,
                  sgemm_stream_t stream) {
-    if (kernel_id < -1 || schedule < 0 || schedule > 2) {
+    if (kernel_id < -1 || schedule < 0 || schedule > 3) {
         std::snprintf(t_last_error, sizeof(t_last_error), "bad kernel_id %d or schedule %d",
                       kernel_id, schedule);
         return kernel_id < -1 ? SGEMM_ERR_UNSUPPORTED : SGEMM_ERR_INVALID_ARG;
@@ -798,7 +843,7 @@ int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const float* B, i
 
 int sgemm_run_with(int M, int N, int K, const float* A, int lda, const float* B, int ldb,
                    float* C, int ldc, int kernel_id, int schedule, sgemm_stream_t stream) {
-    if (kernel_id < -1 || schedule < 0 || schedule > 2) {
+    if (kernel_id < -1 || schedule < 0 || schedule > 3) {
         std::snprintf(t_last_error, sizeof(t_last_error), "bad kernel_id %d or schedule %d",
                       kernel_id, schedule);
         return kernel_id < -1 ? SGEMM_ERR_UNSUPPORTED : SGEMM_ERR_INVALID_ARG;
@@ -851,7 +896,7 @@ int sgemm_query_config(int M, int N, int K, int lda, int ldb, int ldc, const flo
 int sgemm_schedule_check(int M, int N, int K, int kernel_id, int sms, int ctas_per_sm,
                          int schedule, sgemm_config* out) {
     if (M <= 0 || N <= 0 || K <= 0 || sms <= 0 || ctas_per_sm <= 0 || schedule < 0 ||
-        schedule > 2 || kernel_id < 0 || kernel_id >= static_cast<int>(table().size()))
+        schedule > 3 || kernel_id < 0 || kernel_id >= static_cast<int>(table().size()))
         return SGEMM_ERR_INVALID_ARG;
     Plan p;
     p.entry = kernel_id;
@@ -1067,6 +1112,7 @@ int sgemm_shutdown(void) {
     }
     g_ws.clear();
     shutdown_host_pipes();
+    forget_noalloc_scratch();
     return rc;
 }
 

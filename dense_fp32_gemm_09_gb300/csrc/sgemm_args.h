@@ -28,6 +28,8 @@ struct GemmArgs {
     long long sk_iters;    // sk_tiles * KT: k-tiles shared out over the G CTAs
     int sk_gap;            // virtual k-tiles counted between split tiles (sgemm_sched.cuh)
     int group_m;           // tile rasterisation: tile rows per group
+    int cl_split;          // > 1: every tile is split over a cluster of cl_split CTAs
+                           // that sum their partials in distributed shared memory
 
     float* ws_partial;     // [G][2][BM*BN] partial tiles of split tiles
     int* status;           // device status word (bounded waits that give up)

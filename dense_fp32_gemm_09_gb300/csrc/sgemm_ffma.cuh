@@ -70,6 +70,46 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// Thread-block cluster primitives (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives; shared-memory writes made
+// before the arrive are visible to the whole cluster after the wait.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of cluster_sync, for work between them.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address in the shared::cluster window of the same shared-memory location in
+// the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_address, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_address), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t address) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(address)
+                 : "memory");
+    return v;
+}
+
 // d += x * y elementwise on packed pairs (low 32 bits = column j, high = column
 // j+1); one multiplicand is two adjacent B values, the other one A value in both
 // halves.  The product is commutative; the operand order is a scheduling choice.
@@ -207,7 +247,12 @@ struct FfmaCfg {
     static constexpr int LDBS = BN;
     static constexpr int A_STAGE = BM * LDAS;
     static constexpr int B_STAGE = BK * LDBS;
-    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    // Cluster split: the CTA's partial tile, rows padded by 8 floats so the float4
+    // writes of a quarter-warp (4 rows x 2 adjacent chunks) hit distinct banks.
+    static constexpr int LDP = BN + 8;
+    static constexpr int PART_BYTES = BM * LDP * 4;
+    static constexpr int PIPE_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static constexpr int SMEM_BYTES = PIPE_BYTES > PART_BYTES ? PIPE_BYTES : PART_BYTES;
 
     static_assert(BM == WM * WARPS_M, "BM must equal WM * WARPS_M");
     static_assert(BN == WN * WARPS_N, "BN must equal WN * WARPS_N");
@@ -387,6 +432,101 @@ __device__ __forceinline__ void store_partial(const GemmArgs& a, const CtaWork& 
                    acc.chunk(i, j4));
 }
 
+// Cluster split: rank r of the S CTAs sharing a tile sums rows
+// [r*BM/S, (r+1)*BM/S) of the S partial tiles, held in the CTAs' shared memory,
+// in rank order (rank q computed the q-th contiguous piece of K, so this is
+// increasing k, as in the stream-K reduction), and stores them to C.  Each
+// thread first issues all the distributed-shared-memory loads of U float4 of
+// the band, then adds and stores them.
+template <class Cfg, int S>
+__device__ __forceinline__ void cluster_band_sum(const GemmArgs& a, const float* part, int tid) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, NT = Cfg::NT, LDP = Cfg::LDP;
+    static_assert(BM % S == 0, "the cluster size divides the tile height");
+    constexpr int ROWS = BM / S;
+    constexpr int CPR = BN / 4;                      // float4 per row
+    constexpr int V4 = ROWS * CPR;                   // float4 in this CTA's band
+    constexpr int PER = (V4 + NT - 1) / NT;          // float4 per thread
+    constexpr int U0 = (32 / S) < 1 ? 1 : 32 / S;    // at most 32 loads in flight
+    constexpr int U = PER < U0 ? PER : U0;
+    const uint32_t rank = cluster_ctarank();
+    const int tile = blockIdx.x / S;
+    int m0, n0;
+    tile_origin(a, a.dp_tiles + tile, BM, BN, m0, n0);
+    const uint32_t base = smem_addr(part);
+    uint32_t peer[S];
+#pragma unroll
+    for (int q = 0; q < S; ++q) peer[q] = map_to_rank(base, static_cast<uint32_t>(q));
+    const int row0 = static_cast<int>(rank) * ROWS;
+    for (int e0 = 0; e0 < PER; e0 += U) {
+        float4 v[U][S];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = (e0 + u) * NT + tid;
+            if ((V4 % NT == 0 || e < V4) && e0 + u < PER) {
+                const int rr = row0 + e / CPR, cc = (e % CPR) * 4;
+                const uint32_t off = static_cast<uint32_t>((rr * LDP + cc) * 4);
+#pragma unroll
+                for (int q = 0; q < S; ++q) v[u][q] = ld_cluster_f4(peer[q] + off);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = (e0 + u) * NT + tid;
+            if ((V4 % NT == 0 || e < V4) && e0 + u < PER) {
+                float4 t = v[u][0];
+#pragma unroll
+                for (int q = 1; q < S; ++q) {
+                    t.x += v[u][q].x;
+                    t.y += v[u][q].y;
+                    t.z += v[u][q].z;
+                    t.w += v[u][q].w;
+                }
+                v[u][0] = t;
+            }
+        }
+        // After the last batch every value this thread reads from its peers is
+        // in registers: tell the cluster so (the matching wait is at the end).
+        if (e0 + U >= PER) cluster_arrive();
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = (e0 + u) * NT + tid;
+            if ((V4 % NT == 0 || e < V4) && e0 + u < PER) {
+                const int gm = m0 + row0 + e / CPR, gn = n0 + (e % CPR) * 4;
+                if (gm < a.M && gn < a.N) store_c4(a, a.C + gm * a.ldc, gn, v[u][0]);
+            }
+        }
+    }
+}
+
+// The end of a cluster-split CTA: its partial tile goes to its own shared memory
+// (the pipeline slices are free by now), the cluster synchronises, each CTA sums
+// its band of rows over the cluster, and a second cluster barrier (arrive once
+// the peers' values are read, wait before exit) keeps every CTA's shared memory
+// alive until all peers have read it.  Every thread of every CTA of the cluster
+// reaches both barriers: cluster_band_sum arrives exactly once per thread (its
+// batch loop runs at least once, PER >= 1), and S is 2, 4 or 8.
+template <class Cfg, class AccT>
+__device__ __forceinline__ void cluster_sum_store(const GemmArgs& a, const AccT& acc,
+                                                  float* part, int a_row0, int b_col0,
+                                                  int tid) {
+    constexpr int TM = Cfg::TM, TN = Cfg::TN, LR = Cfg::LR, LC = Cfg::LC, LDP = Cfg::LDP;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j4 = 0; j4 < TN / 4; ++j4)
+            *reinterpret_cast<float4*>(part + (a_row0 + i * LR) * LDP + b_col0 + j4 * LC * 4) =
+                acc.chunk(i, j4);
+    cluster_sync();
+    switch (a.cl_split) {
+        case 2: cluster_band_sum<Cfg, 2>(a, part, tid); break;
+        case 4: cluster_band_sum<Cfg, 4>(a, part, tid); break;
+        case 8: cluster_band_sum<Cfg, 8>(a, part, tid); break;
+        default: cluster_arrive(); break;
+    }
+    cluster_wait();
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const GemmArgs a) {
     extern __shared__ __align__(16) float smem[];
@@ -410,14 +550,22 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const Ge
     const int a_row0 = warp_m * Cfg::WM + lr;
     const int b_col0 = warp_n * Cfg::WN + lc * 4;
 
-    const CtaWork w = make_work(a, blockIdx.x);
-    if (w.total <= 0) return;
+    // A cluster-split CTA always goes on to the cluster barriers at the end.
+    const bool cl = a.cl_split > 1;
+    const CtaWork w = cl ? make_cluster_work(a, blockIdx.x) : make_work(a, blockIdx.x);
+    if (w.total <= 0 && !cl) return;
 
     float* const sA0 = smem;
     float* const sB0 = smem + STAGES * Cfg::A_STAGE;
 
     Cursor ld;
-    ld.seek(w, 0);
+    if (cl) {
+        const int t = static_cast<int>(blockIdx.x) >> (__ffs(a.cl_split) - 1);
+        const long long tb = static_cast<long long>(t) * w.KT;
+        ld.set_piece(t, static_cast<int>(w.u0 - tb), static_cast<int>(w.u1 - tb));
+    } else {
+        ld.seek(w, 0);
+    }
     Cursor cp = ld;
 
     // Launched as a programmatic dependent of the stream's previous kernel: the
@@ -463,11 +611,15 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const Ge
         stage = (stage + 1 == STAGES) ? 0 : stage + 1;
 
         if (cp.kt + 1 == cp.kt_end) {
-            if (cp.kt_begin == 0 && cp.kt_end == w.KT)
-                store_tile<Cfg>(a, acc, m0c, n0c, a_row0, b_col0);
-            else
-                store_partial<Cfg>(a, w, cp, acc, a_row0, b_col0);
-            acc.zero();
+            // A cluster-split CTA holds one piece of one tile: its sum stays in
+            // the registers for the cluster sum after the loop.
+            if (!cl) {
+                if (cp.kt_begin == 0 && cp.kt_end == w.KT)
+                    store_tile<Cfg>(a, acc, m0c, n0c, a_row0, b_col0);
+                else
+                    store_partial<Cfg>(a, w, cp, acc, a_row0, b_col0);
+                acc.zero();
+            }
             cp.advance(w);
             if (cp.c < w.total) tile_origin(a, cp.tile, Cfg::BM, Cfg::BN, m0c, n0c);
         } else {
@@ -475,6 +627,7 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const Ge
         }
     }
     cp_async_wait<0>();
+    if (cl) cluster_sum_store<Cfg>(a, acc, smem, a_row0, b_col0, tid);
     // Lets a programmatic dependent launch (the stream-K reduction) get scheduled
     // now; it still waits for this whole grid to finish before reading results.
     asm volatile("griddepcontrol.launch_dependents;");

@@ -35,6 +35,10 @@ int check_operands(int transa, int transb, int M, int N, int K, const float* A, 
 // Destroys the host-buffer entry point's streams and events (sgemm_shutdown).
 void shutdown_host_pipes();
 
+// Drops the cached device addresses of sgemm_run_noalloc's static scratch
+// (sgemm_shutdown); the next call looks them up again.
+void forget_noalloc_scratch();
+
 // 3xTF32 tensor-core path (sgemm_tf32x3.cu).
 size_t tf32x3_workspace_bytes(int M, int N, int K);
 // write_ahi = false leaves the Ahi region unwritten: the multiply then takes hi

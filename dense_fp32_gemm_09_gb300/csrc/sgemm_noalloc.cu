@@ -9,11 +9,14 @@
 // that scratch from one fixed array compiled into the library instead of from
 // a workspace it would otherwise allocate.
 //
-// The array is a file-scope __device__ variable: every GPU that loads the
-// library holds its kNoAllocScratchBytes until the process exits.  In host code
-// the array's name is only a host-side stand-in, so its device address is
-// looked up once per device with cudaGetSymbolAddress (the first call on a
-// device does this, with that device current) and passed to the kernels.
+// The array is a file-scope __device__ variable.  In host code the array's
+// name is only a host-side stand-in, so its device address is looked up once
+// per device with cudaGetSymbolAddress (the first call on a device that needs
+// scratch does this, with that device current) and passed to the kernels.
+// Under CUDA's lazy module loading that lookup is what loads this file's module
+// and with it reserves the array on the device; the device then holds it until
+// the process exits.  sgemm_shutdown forgets the addresses (they belong to the
+// primary context of each device), so the next call looks them up again.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -67,6 +70,12 @@ int scratch_address(void** out) {
 }
 
 }  // namespace
+
+void forget_noalloc_scratch() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int d = 0; d < kMaxDevices; ++d) g_scratch_addr[d] = nullptr;
+}
+
 }  // namespace sgemm
 
 extern "C" int sgemm_run_noalloc(int M, int N, int K, const float* A, int lda, const float* B,

@@ -33,7 +33,13 @@ __global__ void __launch_bounds__(kReduceThreads) sk_reduce_kernel(const GemmArg
     const int g0 = sk_owner(a, tb);
     const int g1 = sk_owner(a, tb + a.KT - 1);
     const int n = g1 - g0 + 1;  // contributors, in increasing k order
-    if (n <= 1) return;         // one CTA held the whole K range and stored the tile itself
+    if (n <= 1) {
+        // One CTA held the whole K range and stored the tile itself.  Still wait
+        // for the main kernel: a kernel launched as a programmatic dependent of
+        // this one relies on the main kernel having completed when this grid has.
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
     const long long tile_floats = static_cast<long long>(bm) * bn;
     for (int i = threadIdx.x; i < n; i += kReduceThreads) {
         const int gg = g0 + i;

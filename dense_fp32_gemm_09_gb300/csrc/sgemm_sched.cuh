@@ -82,6 +82,29 @@ __host__ __device__ __forceinline__ CtaWork make_work(const GemmArgs& a, int g) 
     return w;
 }
 
+// make_work for a cluster split (a.cl_split = S, a power of two): CTA g = t*S + r
+// holds slices [floor(KT*r/S), floor(KT*(r+1)/S)) of tile t, which is what
+// make_work gives for G = T*S and no data-parallel tiles, with shifts in place
+// of its 64-bit divisions (the host-side schedule check compares the two).
+__host__ __device__ __forceinline__ CtaWork make_cluster_work(const GemmArgs& a, int g) {
+    int sh = 0;
+    while ((1 << sh) < a.cl_split) ++sh;
+    const long long t = g >> sh, r = g & (a.cl_split - 1);
+    const long long tb = t * a.KT;
+    CtaWork w;
+    w.g = g;
+    w.G = a.grid;
+    w.KT = a.KT;
+    w.dp_tiles = 0;
+    w.n_dp = 0;
+    w.sk_iters = a.sk_iters;
+    w.u0 = tb + ((a.KT * r) >> sh);
+    w.u1 = tb + ((a.KT * (r + 1)) >> sh);
+    w.dp_iters = 0;
+    w.total = w.u1 - w.u0;
+    return w;
+}
+
 // Partial-tile slot (0 or 1) CTA w uses for split tile t: a CTA's stream-K range
 // is shorter than one tile's K range plus one gap, so it touches at most two
 // split tiles.
@@ -113,10 +136,17 @@ struct Cursor {
             kt_end = static_cast<int>((w.u1 < te ? w.u1 : te) - tb);
         }
     }
+    // Piece [kb, ke) of tile `t` as the whole list (a cluster-split CTA).
+    __host__ __device__ __forceinline__ void set_piece(int t, int kb, int ke) {
+        c = 0;
+        tile = t;
+        kt = kt_begin = kb;
+        kt_end = ke;
+    }
     __host__ __device__ __forceinline__ void advance(const CtaWork& w) {
         ++c;
         ++kt;
-        if (kt >= kt_end) seek(w, c);
+        if (kt >= kt_end && c < w.total) seek(w, c);
     }
 };
 
@@ -211,18 +241,71 @@ inline int choose_sk_gap(GemmArgs& a, double store, int forced) {
     return best;
 }
 
+// Cluster split (cl_split = S > 1).  Every tile's K range is cut into S
+// contiguous pieces, one per CTA, and the S CTAs of a tile are one thread-block
+// cluster: CTAs t*S .. t*S+S-1 hold tile t, rank r holding the r-th piece.  It is
+// the stream-K partition above with G = T*S, no data-parallel tiles and no gap,
+// which gives CTA t*S+r the slices [floor(KT*r/S), floor(KT*(r+1)/S)) of tile t.
+// The partials are summed inside the cluster in rank (= k) order, so no
+// workspace and no second launch are needed.
+constexpr int kMaxCluster = 8;        // portable cluster size
+constexpr int kMaxClusterGrid = 1 << 22;
+
+// Automatic cluster size for T tiles of KT slices on a resident grid of gmax
+// CTAs (occ per SM), 0 for none.  Chosen from CUDA-event step times on GB300
+// (L2 flushed before each step; 128^3 .. 1536^3 cubes and narrow shapes such as
+// 2048x256x256 and 4096x128x256), where the rule below picked the fastest of
+// S = 0, 2, 4, 8 or came within 5 % of it:
+//   * at least 2 slices per CTA, and 4 for clusters of 8 (one- and two-slice
+//     pieces in clusters of 8 lost to clusters of 4 at 128^3 .. 384^3);
+//   * one resident wave (T*S <= gmax); clusters of 8 of an entry with 4 or more
+//     CTAs per SM may take up to 1.35 waves (640^3 on 64 x 64 tiles);
+//   * an entry with one CTA per SM keeps stream-K when the cluster grid would
+//     leave more than a tenth of stream-K's grid idle (1024^3 on 256 x 128
+//     tiles: 128 clustered CTAs ran 53.6 us, 152 stream-K CTAs 51.5 us).
+inline int auto_cluster_size(long long T, int KT, long long gmax, int occ, int cap) {
+    long long g_sk = T * KT / kMinSkIters;   // stream-K's grid for the same tiles
+    if (g_sk < T) g_sk = T;
+    if (g_sk > gmax) g_sk = gmax;
+    for (int S = cap; S >= 2; S /= 2) {
+        const int min_slices = S >= 8 ? 4 : 2;
+        if (KT < static_cast<long long>(S) * min_slices) continue;
+        const double waves = (S >= 8 && occ >= 4) ? 1.35 : 1.0;
+        if (static_cast<double>(T * S) > waves * static_cast<double>(gmax)) continue;
+        if (occ == 1 && static_cast<double>(T * S) < 0.9 * static_cast<double>(g_sk)) return 0;
+        return S;
+    }
+    return 0;
+}
+
+// Cluster size for T tiles of KT slices: the largest power of two S <= cap with
+// at least min_slices slices per CTA and T*S <= gmax (0 when below 2).
+inline int cluster_size_for(long long T, int KT, long long gmax, int cap, int min_slices) {
+    int s = 1;
+    while (2 * s <= cap && static_cast<long long>(KT) >= 2LL * s * min_slices &&
+           T * 2 * s <= gmax)
+        s *= 2;
+    return s >= 2 ? s : 0;
+}
+
 // Fills the schedule fields of `a` (a.M, a.N, a.K set) for BM x BN x BK tiles on
 // `sms` SMs holding `occ` CTAs each.  schedule: 0 automatic, 1 data-parallel
-// only, 2 stream-K on any partial wave that has at least one k-slice per CTA.
+// only, 2 stream-K on any partial wave that has at least one k-slice per CTA,
+// 3 cluster split of every tile (see above) wherever K has a slice per CTA.
 // store_slices: cost of storing one tile in k-slices (0: equal stream-K ranges,
 // no gap); forced_gap >= 0 overrides the gap choice where it is allowed;
 // group_m > 0 sets the raster group height (0: chosen from the tile shape).
+// cluster_max: largest cluster the kernel can sum in (0: none); forced_cluster:
+// -1 automatic, 0 never, S >= 2 clusters of the largest power of two up to S
+// that gives every CTA a slice.
 inline SchedSizes plan_schedule(GemmArgs& a, int bm, int bn, int bk, int sms, int occ,
                                 int schedule, double store_slices = 0.0,
-                                int forced_gap = -1, int group_m = 0) {
+                                int forced_gap = -1, int group_m = 0, int cluster_max = 0,
+                                int forced_cluster = -1) {
     a.tiles_m = (a.M + bm - 1) / bm;
     a.tiles_n = (a.N + bn - 1) / bn;
     a.KT = (a.K + bk - 1) / bk;
+    a.cl_split = 0;
     const long long T = static_cast<long long>(a.tiles_m) * a.tiles_n;
     long long Gmax = static_cast<long long>(sms) * occ;
     if (Gmax > kMaxSkTiles) Gmax = kMaxSkTiles;
@@ -237,6 +320,30 @@ inline SchedSizes plan_schedule(GemmArgs& a, int bm, int bn, int bk, int sms, in
         while (group_m < 4096 && group_m * 1.4142135623730951 < r) group_m *= 2;
     }
     a.group_m = a.tiles_m < group_m ? a.tiles_m : group_m;
+
+    // Cluster split: forced (schedule 3 or a forced size), or automatic for
+    // problems of less than one resident wave of tiles (auto_cluster_size).
+    if (cluster_max >= 2 && schedule != 1 && schedule != 2 && forced_cluster != 0) {
+        const int cap = cluster_max < kMaxCluster ? cluster_max : kMaxCluster;
+        int S = 0;
+        if (forced_cluster >= 2 || schedule == 3) {
+            const int want = forced_cluster >= 2 ? forced_cluster : cap;
+            S = cluster_size_for(T, a.KT, kMaxClusterGrid, want < cap ? want : cap, 1);
+        } else if (T < Gmax) {
+            S = auto_cluster_size(T, a.KT, Gmax, occ, cap);
+        }
+        if (S >= 2) {
+            a.grid = static_cast<int>(T * S);
+            a.dp_tiles = 0;
+            a.sk_tiles = static_cast<int>(T);
+            a.sk_iters = T * a.KT;
+            a.sk_gap = 0;
+            a.cl_split = S;
+            SchedSizes z;
+            z.split = S;
+            return z;
+        }
+    }
 
     long long G, dp, sk;
     if (T >= Gmax) {

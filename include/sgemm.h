@@ -84,13 +84,20 @@ typedef struct {
     int packed;            /* sgemm_run copies A (bit 0) / B (bit 1) to aligned buffers first */
     int sk_gap;            /* stream-K: k-slices of store time counted between split tiles
                               when the K ranges are shared out (0: equal ranges) */
+    int cluster;           /* cluster split: CTAs per tile, one thread-block cluster each,
+                              summing their partial tiles in distributed shared memory in
+                              a fixed order, in the same launch (0: not used) */
 } sgemm_config;
 
 /* C = A.B on `stream`.  One kernel launch, plus a second, short reduction launch
  * when the schedule splits the K range of some tiles between CTAs (stream-K);
  * the partial tiles then go to a library-owned device workspace (allocated on
  * first use per device and stream with the stream-ordered allocator, grown when
- * a larger one is needed, freed by sgemm_shutdown).  Large problems (M*N*K >=
+ * a larger one is needed, freed by sgemm_shutdown).  Problems of less than one
+ * resident wave of tiles may instead split every tile's K range over a
+ * thread-block cluster of 2, 4 or 8 CTAs that sum their partial tiles in
+ * distributed shared memory, in k order, inside the one launch; that needs no
+ * workspace (sgemm_query_config reports it as `cluster`).  Large problems (M*N*K >=
  * 2^31) whose A or B rows are not 16-byte aligned are first copied row by row
  * into aligned buffers in that workspace (one more launch per copied operand),
  * so they run on the 16-byte / TMA kernels (the copy moves values, not sums: the
@@ -139,17 +146,31 @@ SGEMM_API int sgemm_run_ws(int M, int N, int K, const float* A, int lda, const f
  * their whole device memory budget up front).  The source pages have no
  * counterpart to this entry point: it exists only for such callers.
  *
- * When the schedule splits tiles between CTAs, the partial tiles go to one
- * static __device__ array of SGEMM_NOALLOC_SCRATCH_BYTES compiled into the
- * library; every GPU that loads the library holds that array until the process
- * exits.  A problem that would need more scratch than that is rejected with
+ * When the schedule splits tiles between CTAs through a workspace (stream-K),
+ * the partial tiles go to one static __device__ array of
+ * SGEMM_NOALLOC_SCRATCH_BYTES compiled into the library; problems whose tiles
+ * are split inside thread-block clusters, or not split at all, use no scratch.
+ * A problem that would need more scratch than the array holds is rejected with
  * SGEMM_ERR_WORKSPACE and a message in sgemm_last_error(); nothing is launched.
- * The first call on each device looks up the array's device address (with that
- * device current); make that first call before any stream capture begins.  All
- * calls on a device share the array, so calls that can overlap on the GPU
+ *
+ * Set-up: the first call on a device that needs the scratch looks up the
+ * array's device address (with that device current).  Under CUDA's default lazy
+ * module loading that lookup is also what loads the library module holding the
+ * array, so that first call reserves SGEMM_NOALLOC_SCRATCH_BYTES of device
+ * memory (as the first launch of any kernel loads that kernel's code); from
+ * then on the device holds the array until the process exits, and later calls
+ * allocate nothing.  Make that first call at set-up time, before any stream
+ * capture begins and before the device's memory budget is fixed.  The address
+ * is kept per device index for the primary context and looked up again after
+ * sgemm_shutdown.
+ *
+ * All calls on a device share the array, so calls that can overlap on the GPU
  * (e.g. on different streams without ordering between them) race and must not
- * be issued; calls ordered on one stream are fine.  A, B, C and `stream` are as
- * for sgemm_run. */
+ * be issued; calls ordered on one stream are fine.  Like sgemm_run_ws (it is
+ * that call with the static array as workspace), it never copies misaligned
+ * operands to aligned buffers first, so for such operands it may run another
+ * tile-table entry than sgemm_run and round differently, within the same bound.
+ * A, B, C and `stream` are as for sgemm_run. */
 SGEMM_API int sgemm_run_noalloc(int M, int N, int K, const float* A, int lda, const float* B,
                                 int ldb, float* C, int ldc, sgemm_stream_t stream);
 
@@ -166,7 +187,10 @@ SGEMM_API int sgemm_workspace_size(int M, int N, int K, int lda, int ldb, int ld
 
 /* As sgemm_run, forcing tile-table entry `kernel_id` (for tests and tuning) and a
  * schedule: `schedule` 0 = automatic, 1 = data-parallel only, 2 = stream-K on the
- * last partial wave whenever it has at least one k-tile per CTA.  Returns
+ * last partial wave whenever it has at least one k-tile per CTA, 3 = every tile
+ * split over a cluster of the largest power of two up to 8 CTAs that leaves each
+ * a k-tile (the TMA-fed entries, which cannot sum in a cluster, plan as for 0).
+ * Returns
  * SGEMM_ERR_UNSUPPORTED if that entry cannot serve these operands (e.g. a
  * 16-byte-load entry for unaligned operands). */
 SGEMM_API int sgemm_run_with(int M, int N, int K, const float* A, int lda, const float* B, int ldb,

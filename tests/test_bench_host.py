@@ -26,3 +26,17 @@ def test_code_hash_ignores_comments_but_not_code():
 def test_recorded_traffic_needs_a_matching_entry_and_workload():
     assert bench.recorded_traffic("no_such_entry", "sgemm_4096") is None
     assert bench.recorded_traffic("256x128x64_t8x16_s2_f2_v4", "no_such_workload") is None
+
+
+def test_reference_arm_prints_the_gpu_arms_config(capsys):
+    """Both arms of a workload carry the same `config` (the GPU-only details of the
+    plan go to `plan`), so their lines can be matched key for key."""
+    import argparse
+    import json
+    w = bench.WORKLOADS["sgemm_256"]
+    args = argparse.Namespace(steps=1, warmup=0, gpus=1)
+    assert bench.run_reference(args, w) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.workload_config(w, 1)
+    assert set(line["config"]) == {"workload", "M", "N", "K", "l2", "parallelism"}

@@ -55,7 +55,7 @@ def padded(torch, X, pad, offset=0):
 
 
 @pytest.mark.parametrize("name", ["sgemm_256", "sgemm_1024", "sgemm_2048",
-                                  "sgemm_ragged_3001x2047x1999"])
+                                  "sgemm_ragged_3001x2047x1999", "sgemm_4096"])
 def test_workload_full_parity(cuda, oracle_mod, name):
     torch = cuda
     A, B = make_inputs(name)
@@ -66,15 +66,22 @@ def test_workload_full_parity(cuda, oracle_mod, name):
     assert err <= tolerance(A, B), (name, err, tolerance(A, B))
 
 
-@pytest.mark.parametrize("name", ["sgemm_4096", "sgemm_8192", "sgemm_tall_16384x64x4096"])
+@pytest.mark.parametrize("name", ["sgemm_8192", "sgemm_tall_16384x64x4096"])
 def test_workload_sampled_rows(cuda, oracle_mod, name):
+    """256 seeded rows plus the first and the last, and two rows in every band of
+    BM rows (one CTA tile high), so that every tile, the split ones included, has
+    rows in the sample; each sampled row is compared over all N columns."""
     torch = cuda
     w = WORKLOADS[name]
     A, B = make_inputs(name)
     C = sgemm(A.cuda(), B.cuda())
     torch.cuda.synchronize()
+    bm = sgemm_query_config(w.M, w.N, w.K)["bm"]
+    bands = [min(r, w.M - 1) for b in range(0, w.M, bm)
+             for r in (b + (b // bm * 37) % bm, b + bm - 1)]
     rng = np.random.default_rng(12345)
-    rows = np.unique(np.concatenate([[0, w.M - 1], rng.integers(0, w.M, 48)])).astype(np.int32)
+    rows = np.unique(np.concatenate([[0, w.M - 1], rng.integers(0, w.M, 256),
+                                     bands])).astype(np.int32)
     ref = oracle_mod.gemm_f64_rows(A.numpy(), B.numpy(), rows)
     got = C[torch.from_numpy(rows.astype(np.int64)).cuda()].cpu().numpy().astype(np.float64)
     err = np.max(np.abs(got - ref))
@@ -105,7 +112,7 @@ def _ids():
 
 
 @pytest.mark.parametrize("kname", _ids())
-@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("schedule", [1, 2, 3])
 def test_each_kernel_ragged_shapes(cuda, oracle_mod, kname, schedule):
     torch = cuda
     table = {k["name"]: k for k in kernel_table()}
@@ -238,6 +245,7 @@ def test_stream_k_gap_parity(cuda, oracle_mod, monkeypatch, gap):
     oracle, writes nothing outside C, repeats bit for bit, and reports the gap."""
     torch = cuda
     monkeypatch.setenv("SGEMM_SK_GAP", gap)
+    monkeypatch.setenv("SGEMM_CLUSTER", "0")   # the stream-K form of every split
     used = 0
     for (M, N, K) in [(1024, 1024, 1024), (700, 900, 2500), (1001, 517, 1999)]:
         A, B = random_pair(M, N, K, seed=M + N + K)

@@ -46,7 +46,8 @@ def test_stream_k_balances_a_partial_last_wave(lib):
     assert cfg.sk_tiles == 0 and cfg.grid == 152
 
 
-def test_small_problem_splits_k(lib):
+def test_small_problem_splits_k(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_CLUSTER", "0")   # the stream-K form of the split
     table = [lib.sgemm_kernel_name(i).decode() for i in range(lib.sgemm_num_kernels())]
     kid = table.index("128x256x32_t8x16_s4_f2_v4")
     cfg = _cfg()
@@ -138,6 +139,7 @@ def test_gap_choice_minimises_the_critical_path(lib, monkeypatch, M, N, K, name,
     """The planner's gap is the smallest one with the shortest longest-CTA time,
     the partition rebuilt here position by position."""
     monkeypatch.delenv("SGEMM_SK_GAP", raising=False)
+    monkeypatch.setenv("SGEMM_CLUSTER", "0")
     cfg = _cfg()
     assert lib.sgemm_schedule_check(M, N, K, _kid(lib, name), 152, occ, 0,
                                     ctypes.byref(cfg)) == 0
@@ -198,3 +200,135 @@ def test_gap_memo_is_order_independent(lib, monkeypatch):
     monkeypatch.delenv("SGEMM_SK_GAP")
     assert gaps(cases[::-1]) == first
     assert any(g > 0 for g in first.values()) and any(g == 0 for g in first.values())
+
+
+# --------------------------------------------------------------------------
+# cluster split: each tile's K range cut into S pieces, one per CTA of a
+# thread-block cluster, summed in distributed shared memory
+# --------------------------------------------------------------------------
+
+
+def _is_tma(lib, kid):
+    return lib.sgemm_kernel_name(kid).decode().endswith("_tma")
+
+
+def test_cluster_schedule_covers_each_slice_once(lib, monkeypatch):
+    """schedule 3: every cp.async entry splits every tile over a cluster whenever
+    K has a slice for each CTA; the walk checks each (tile, slice) once, pieces in
+    rank order inside tile g / S, and the cluster grid."""
+    monkeypatch.delenv("SGEMM_CLUSTER", raising=False)
+    n = lib.sgemm_num_kernels()
+    seen = set()
+    for kid, (M, N, K), (sms, occ) in itertools.product(range(n), SHAPES, MACHINES):
+        cfg = _cfg()
+        rc = lib.sgemm_schedule_check(M, N, K, kid, sms, occ, 3, ctypes.byref(cfg))
+        assert rc == 0, (kid, M, N, K, sms, occ, lib.sgemm_last_error())
+        KT = -(-K // cfg.bk)
+        if _is_tma(lib, kid):
+            assert cfg.cluster == 0
+            continue
+        want = 1
+        while 2 * want <= min(8, KT):
+            want *= 2
+        assert cfg.cluster == (want if want >= 2 else 0), (kid, M, N, K, cfg.cluster)
+        if cfg.cluster:
+            assert cfg.grid == cfg.tiles * cfg.cluster and cfg.sk_tiles == cfg.tiles
+            assert cfg.split_k == cfg.cluster and cfg.sk_gap == 0
+            seen.add(cfg.cluster)
+    assert seen == {2, 4, 8}
+
+
+@pytest.mark.parametrize("S", [2, 4, 8])
+def test_forced_cluster_size(lib, monkeypatch, S):
+    """SGEMM_CLUSTER=S asks for clusters of up to S CTAs: the largest power of two
+    at most S that still gives every CTA a slice (none below 2)."""
+    monkeypatch.setenv("SGEMM_CLUSTER", str(S))
+    for kid in range(lib.sgemm_num_kernels()):
+        for (M, N, K) in [(256, 256, 256), (3001, 2047, 1999), (65, 63, 17), (1, 1, 1)]:
+            for schedule in (0, 3):
+                cfg = _cfg()
+                assert lib.sgemm_schedule_check(M, N, K, kid, 152, 1, schedule,
+                                                ctypes.byref(cfg)) == 0
+                KT = -(-K // cfg.bk)
+                cap = 1
+                while 2 * cap <= min(S, KT):
+                    cap *= 2
+                expect = 0 if _is_tma(lib, kid) or cap < 2 else cap
+                if schedule == 0 and expect == 0 and not _is_tma(lib, kid):
+                    expect = cfg.cluster   # falls back to the automatic plan
+                assert cfg.cluster == expect, (kid, M, N, K, schedule, cfg.cluster)
+
+
+def test_no_cluster_when_disabled_or_forced_otherwise(lib, monkeypatch):
+    monkeypatch.setenv("SGEMM_CLUSTER", "0")
+    for kid in range(lib.sgemm_num_kernels()):
+        for schedule in (0, 1, 2, 3):
+            cfg = _cfg()
+            assert lib.sgemm_schedule_check(256, 256, 256, kid, 152, 1, schedule,
+                                            ctypes.byref(cfg)) == 0
+            assert cfg.cluster == 0
+    monkeypatch.delenv("SGEMM_CLUSTER")
+    for kid in range(lib.sgemm_num_kernels()):
+        for schedule in (1, 2):
+            cfg = _cfg()
+            assert lib.sgemm_schedule_check(256, 256, 256, kid, 152, 1, schedule,
+                                            ctypes.byref(cfg)) == 0
+            assert cfg.cluster == 0
+
+
+def _auto_cluster(T, KT, gmax, occ):
+    """The automatic rule, restated: the largest S in 8, 4, 2 with at least 2
+    slices per CTA (4 for S = 8) and one resident wave (1.35 for S = 8 when the
+    entry keeps 4 or more CTAs per SM); entries with one CTA per SM keep stream-K
+    when the cluster grid is under 0.9 of stream-K's."""
+    g_sk = min(max(T * KT // 4, T), gmax)
+    for S in (8, 4, 2):
+        if KT < S * (4 if S == 8 else 2):
+            continue
+        if T * S > (1.35 if S == 8 and occ >= 4 else 1.0) * gmax:
+            continue
+        if occ == 1 and T * S < 0.9 * g_sk:
+            return 0
+        return S
+    return 0
+
+
+def test_automatic_cluster_rule(lib, monkeypatch):
+    """schedule 0 picks a cluster split by the measured rule for problems of less
+    than one resident wave of tiles; never for TMA-fed entries."""
+    monkeypatch.delenv("SGEMM_CLUSTER", raising=False)
+    used = set()
+    for kid in range(lib.sgemm_num_kernels()):
+        for (M, N, K) in SHAPES + [(128, 128, 128), (384, 384, 384), (512, 512, 512),
+                                   (640, 640, 640), (768, 768, 768), (1536, 1536, 1536),
+                                   (2048, 256, 256), (4096, 128, 256)]:
+            for sms, occ in MACHINES + [(152, 4), (152, 8)]:
+                cfg = _cfg()
+                assert lib.sgemm_schedule_check(M, N, K, kid, sms, occ, 0,
+                                                ctypes.byref(cfg)) == 0
+                T, KT, gmax = cfg.tiles, -(-K // cfg.bk), min(sms * occ, 16384)
+                expect = 0 if (_is_tma(lib, kid) or T >= gmax) else _auto_cluster(T, KT, gmax,
+                                                                                   occ)
+                assert cfg.cluster == expect, (kid, M, N, K, sms, occ, cfg.cluster, expect)
+                used.add(expect)
+    assert used == {0, 2, 4, 8}
+
+
+@pytest.mark.parametrize("M,N,K,name,occ,S", [
+    (128, 128, 128, "32x32x16_t4x4_s3_f2_v4", 8, 4),
+    (256, 256, 256, "32x32x16_t4x4_s3_f2_v4", 8, 4),
+    (384, 384, 384, "32x32x16_t4x4_s3_f2_v4", 8, 4),
+    (512, 512, 512, "64x64x16_t8x8_s3_f2_v4", 4, 8),
+    (640, 640, 640, "64x64x16_t8x8_s3_f2_v4", 4, 8),
+    (768, 768, 768, "64x64x16_t8x8_s3_f2_v4", 4, 4),
+    (1024, 1024, 1024, "256x128x32_t8x16_s4_f2_v4", 1, 0),
+    (1536, 1536, 1536, "256x128x32_t8x16_s4_f2_v4", 1, 2),
+    (4096, 128, 256, "256x128x64_t8x16_s2_f2_v4", 1, 2),
+])
+def test_measured_cluster_choices(lib, monkeypatch, M, N, K, name, occ, S):
+    """The cluster sizes of the timed shapes on 152 SMs."""
+    monkeypatch.delenv("SGEMM_CLUSTER", raising=False)
+    cfg = _cfg()
+    assert lib.sgemm_schedule_check(M, N, K, _kid(lib, name), 152, occ, 0,
+                                    ctypes.byref(cfg)) == 0
+    assert cfg.cluster == S

@@ -5,10 +5,18 @@ unbounded time, and some processes fix their device memory budget up front).
 It runs the same kernels as sgemm_run but takes the stream-K partial tiles from
 a static array compiled into the library.  Checked here through the C ABI:
 two calls in a row (the second one finds the array dirty from the first) must
-agree with sgemm_run within the parity tolerance of the other GPU tests, and
-must not change the device's free memory.  This file is collected last so that
-a failure here comes after every other test has run.
+agree with the fp64 oracle and with sgemm_run within the parity tolerance of
+the other GPU tests, and must not change the device's free memory.  A fresh
+process with lazy module loading checks the documented set-up: the first call
+that needs the scratch reserves at most the array (plus the code of the
+module that holds it), later calls nothing.  This file is collected last so
+that a failure here comes after every other test has run.
 """
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 
@@ -23,7 +31,7 @@ def tolerance(A, B):
 
 
 @pytest.mark.parametrize("case", ["sgemm_1024", "sgemm_ragged_3001x2047x1999", "small_dp"])
-def test_noalloc_matches_sgemm_run_twice(cuda, case):
+def test_noalloc_matches_sgemm_run_twice(cuda, oracle_mod, case):
     torch = cuda
     lib = load()
     if case == "small_dp":
@@ -54,9 +62,55 @@ def test_noalloc_matches_sgemm_run_twice(cuda, case):
         assert rc == 0, lib.sgemm_last_error()
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free_before, "device memory changed"
+    exact = oracle_mod.gemm_f64(A.numpy(), B.numpy())
     for out in outs:
         err = float((out - ref).abs().max())
         assert np.isfinite(err) and err <= tolerance(A, B), (case, err)
+        err_oracle = float(np.max(np.abs(out.cpu().numpy().astype(np.float64) - exact)))
+        assert err_oracle <= tolerance(A, B), (case, err_oracle)
+
+
+_FIRST_CALL = r"""
+import json, sys
+sys.path.insert(0, sys.argv[1])
+import torch
+from dense_fp32_gemm_09_gb300 import load, sgemm
+from dense_fp32_gemm_09_gb300.workloads import make_inputs
+lib = load()
+A, B = make_inputs("sgemm_1024")
+dA, dB = A.cuda(), B.cuda()
+ref = sgemm(dA, dB)                 # loads the product kernels' code
+outs = [torch.empty_like(ref) for _ in range(3)]
+torch.cuda.synchronize()
+stream = torch.cuda.current_stream().cuda_stream
+free = [torch.cuda.mem_get_info()[0]]
+for out in outs:
+    rc = lib.sgemm_run_noalloc(1024, 1024, 1024, dA.data_ptr(), 1024, dB.data_ptr(), 1024,
+                               out.data_ptr(), 1024, stream)
+    torch.cuda.synchronize()
+    free.append(torch.cuda.mem_get_info()[0])
+    assert rc == 0, lib.sgemm_last_error()
+print(json.dumps({"free": free, "err": [float((o - ref).abs().max()) for o in outs]}))
+"""
+
+
+def test_first_call_reserves_at_most_the_static_scratch(cuda):
+    """Fresh process, lazy module loading: the first call that needs the scratch
+    may reserve the static array (and the code of the module holding it), at most
+    SGEMM_NOALLOC_SCRATCH_BYTES plus 16 MiB; the second and third calls change
+    nothing; all three results match sgemm_run within the parity bound."""
+    repo = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY")
+    out = subprocess.run([sys.executable, "-c", _FIRST_CALL, repo], env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    res = json.loads(out.stdout.strip().splitlines()[-1])
+    free = res["free"]
+    first = free[0] - free[1]
+    assert 0 <= first <= (40 << 20) + (16 << 20), first
+    assert free[2] == free[1] and free[3] == free[1], free
+    tol = 1e-6 * 1024 * 1.0 * 1.0      # sgemm_1024 draws A, B from uniform [0, 1)
+    assert max(res["err"]) <= tol, res["err"]
 
 
 def test_noalloc_rejects_bad_arguments_like_sgemm_run(cuda):
