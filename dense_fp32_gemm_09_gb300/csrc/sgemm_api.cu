@@ -222,10 +222,21 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
         // 64-deep slices run about 3% faster; 32-deep ones share K out more finely
         // over the stream-K ranges.  The deeper ones win once every CTA gets about
         // 20 of them (measured from 1536^3, where they lose, to 4096x4096x1536).
+        // Among the 64-deep entries the one with double-buffered fragments (128 x
+        // 256) wins once K >= 2048 and its tiles fill at least two waves (4096^3
+        // 65.4 against 64.1 TFLOP/s, 8192^3 66.5 against 64.9); with less than
+        // that the 256 x 128 entry does (2048^3 59.4 against 58.5, 3008 x 2048 x
+        // 2000 55.6 against 54.6).  Of the 32-deep ones the 128 x 256 tile is the
+        // faster (1536^3 53.4 against 52.6, 1024^3 equal).
         const long long slices64 =
             static_cast<long long>((M + 255) / 256) * ((N + 127) / 128) * ((K + 63) / 64);
-        name = (K >= 2048 || slices64 >= 20LL * sms) ? "256x128x64_t8x16_s2_f2_v4"
-                                                     : "256x128x32_t8x16_s4_f2_v4";
+        const long long tiles_w = static_cast<long long>((M + 127) / 128) * ((N + 255) / 256);
+        if (K >= 2048 && tiles_w >= 2LL * sms)
+            name = "128x256x64_t8x16_s2_f2_v4";
+        else if (K >= 2048 || slices64 >= 20LL * sms)
+            name = "256x128x64_t8x16_s2_f2_v4";
+        else
+            name = "128x256x32_t8x16_s4_f2_v4";
     }
     else
         name = "128x256x32_t8x16_s3_f2_v1";

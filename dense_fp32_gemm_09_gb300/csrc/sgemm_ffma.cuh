@@ -226,7 +226,7 @@ struct Acc<TM, TN, true, BOUTER> {
 // ----------------------------------------------------------------------------
 template <int BM_, int BN_, int BK_, int TM_, int TN_, int LR_, int WARPS_M_, int WARPS_N_,
           int STAGES_, int VEC_, int AK_, bool FMA2_, int MINB_, bool PIPE_ = false,
-          int KU_ = 0>
+          int KU_ = 0, int SPREAD_ = 0>
 struct FfmaCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, TM = TM_, TN = TN_;
     static constexpr int LR = LR_, LC = 32 / LR_;
@@ -241,6 +241,10 @@ struct FfmaCfg {
     static constexpr bool PIPE = PIPE_;
     // KU: AK-deep steps per copy of the unrolled slice loop (0: the whole slice).
     static constexpr int KU = KU_ > 0 ? KU_ : BK_ / AK_;
+    // SPREAD > 0: the refill of the next ring slot is cut into up to SPREAD parts
+    // issued at evenly spaced AK-steps of the first loop body of compute_slice,
+    // instead of one burst before it (see compute_slice).
+    static constexpr int SPREAD = SPREAD_;
     // A slice: [BM][BK + PADA] (row stride odd in 16-byte units); B slice: [BK][BN].
     static constexpr int PADA = ((BK / 4) % 2 == 0) ? 4 : 0;
     static constexpr int LDAS = BK + PADA;
@@ -263,7 +267,9 @@ struct FfmaCfg {
     static_assert(STAGES >= 2, "at least two stages");
 };
 
-template <class Cfg>
+// Part p of P of one slice's copies: each thread's copy loops are cut into P
+// contiguous ranges of iterations (P = 1, p = 0: the whole slice).
+template <class Cfg, int P = 1, int p = 0>
 __device__ __forceinline__ void load_slice(const GemmArgs& a, float* sA, float* sB, int m0,
                                            int n0, int k0, int tid) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, NT = Cfg::NT;
@@ -275,9 +281,10 @@ __device__ __forceinline__ void load_slice(const GemmArgs& a, float* sA, float* 
         // A: BM rows x BK/4 chunks of 16 bytes.
         constexpr int CPR = BK / 4;
         constexpr int CHUNKS = BM * CPR;
+        constexpr int JA = (CHUNKS + NT - 1) / NT;
 #pragma unroll
-        for (int e0 = 0; e0 < CHUNKS; e0 += NT) {
-            const int e = e0 + tid;
+        for (int j = JA * p / P; j < JA * (p + 1) / P; ++j) {
+            const int e = j * NT + tid;
             if (CHUNKS % NT == 0 || e < CHUNKS) {
                 const int r = e / CPR, c = (e % CPR) * 4;
                 const bool ok = (r < rows_left) && (c < k_left);
@@ -289,9 +296,10 @@ __device__ __forceinline__ void load_slice(const GemmArgs& a, float* sA, float* 
         // B: BK rows x BN/4 chunks.
         constexpr int CPRB = BN / 4;
         constexpr int CHUNKSB = BK * CPRB;
+        constexpr int JB = (CHUNKSB + NT - 1) / NT;
 #pragma unroll
-        for (int e0 = 0; e0 < CHUNKSB; e0 += NT) {
-            const int e = e0 + tid;
+        for (int j = JB * p / P; j < JB * (p + 1) / P; ++j) {
+            const int e = j * NT + tid;
             if (CHUNKSB % NT == 0 || e < CHUNKSB) {
                 const int r = e / CPRB, c = (e % CPRB) * 4;
                 const bool ok = (r < k_left) && (c < cols_left);
@@ -302,9 +310,10 @@ __device__ __forceinline__ void load_slice(const GemmArgs& a, float* sA, float* 
         }
     } else {
         constexpr int ELEMS = BM * BK;
+        constexpr int JA = (ELEMS + NT - 1) / NT;
 #pragma unroll
-        for (int e0 = 0; e0 < ELEMS; e0 += NT) {
-            const int e = e0 + tid;
+        for (int j = JA * p / P; j < JA * (p + 1) / P; ++j) {
+            const int e = j * NT + tid;
             if (ELEMS % NT == 0 || e < ELEMS) {
                 const int r = e / BK, c = e % BK;
                 const bool ok = (r < rows_left) && (c < k_left);
@@ -313,9 +322,10 @@ __device__ __forceinline__ void load_slice(const GemmArgs& a, float* sA, float* 
             }
         }
         constexpr int ELEMSB = BK * BN;
+        constexpr int JB = (ELEMSB + NT - 1) / NT;
 #pragma unroll
-        for (int e0 = 0; e0 < ELEMSB; e0 += NT) {
-            const int e = e0 + tid;
+        for (int j = JB * p / P; j < JB * (p + 1) / P; ++j) {
+            const int e = j * NT + tid;
             if (ELEMSB % NT == 0 || e < ELEMSB) {
                 const int r = e / BN, c = e % BN;
                 const bool ok = (r < k_left) && (c < cols_left);
@@ -356,10 +366,61 @@ __device__ __forceinline__ void load_b_frag(const float* sB, int b_col0, int k,
         b[j4] = *reinterpret_cast<const float4*>(sB + k * Cfg::LDBS + b_col0 + j4 * Cfg::LC * 4);
 }
 
+// Where the copies of the next slice go while this one is computed.
+struct Refill {
+    uint32_t sa, sb;     // shared-memory addresses of this thread's first A and B chunks
+    const float* ga;     // this thread's first A source of the slice
+    const float* gb;     // this thread's first B source
+    bool on;             // a slice is to be loaded, spread over this one's compute
+};
+
+// Interior slices (every element inside A and B, 16-byte rows): part p of P of
+// this thread's copies, with no bounds checks.  Thread t copies chunk t % CPR of
+// rows t / CPR + j * RS; part p takes j in [p * JA / P, (p + 1) * JA / P).
+template <class Cfg>
+struct InteriorCopy {
+    static constexpr int CPR = Cfg::BK / 4, RS = Cfg::NT / CPR, JA = Cfg::BM / RS;
+    static constexpr int CPRB = Cfg::BN / 4, RSB = Cfg::NT / CPRB, JB = Cfg::BK / RSB;
+    static constexpr bool OK = Cfg::VEC == 4 && Cfg::NT % CPR == 0 && Cfg::BM % RS == 0 &&
+                               Cfg::NT % CPRB == 0 && Cfg::BK % RSB == 0;
+};
+
+template <class Cfg, int P>
+__device__ __forceinline__ void refill_part(const GemmArgs& a, const Refill& rf, int p) {
+    using IC = InteriorCopy<Cfg>;
+    // ceil(J / P) copies per part; the last parts of a loop shorter than P copy less.
+    constexpr int NA = (IC::JA + P - 1) / P, NB = (IC::JB + P - 1) / P;
+    const long long lda = a.lda, ldb = a.ldb;
+    const float* ga = rf.ga + static_cast<long long>(p * NA * IC::RS) * lda;
+    const uint32_t sa = rf.sa + static_cast<uint32_t>(p * NA * IC::RS * Cfg::LDAS * 4);
+#pragma unroll
+    for (int j = 0; j < NA; ++j)
+        if (IC::JA % P == 0 || p * NA + j < IC::JA)
+            cp_async16(sa + j * IC::RS * Cfg::LDAS * 4, ga + j * IC::RS * lda, 16);
+    const float* gb = rf.gb + static_cast<long long>(p * NB * IC::RSB) * ldb;
+    const uint32_t sb = rf.sb + static_cast<uint32_t>(p * NB * IC::RSB * Cfg::LDBS * 4);
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+        if (IC::JB % P == 0 || p * NB + j < IC::JB)
+            cp_async16(sb + j * IC::RSB * Cfg::LDBS * 4, gb + j * IC::RSB * ldb, 16);
+}
+
+// Shared-memory copies landing in one burst at the start of a slice delay the
+// fragment loads behind them: measured on GB300, the 256 x 128 x 64 micro-kernel
+// on resident shared memory keeps the FMA pipe 87 % busy with its per-slice
+// barrier, 80 % when the next slice's cp.async copies (L2 hits) are issued
+// before the slice and 86 % when they are issued in 8 parts over its first half.
+// With SPREAD = P > 0 an interior refill is issued in P parts at evenly spaced
+// AK-steps of the slice (P / H of them in each of the H loop bodies).
 template <class Cfg, class AccT>
 __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, int a_row0,
-                                              int b_col0, AccT& acc) {
+                                              int b_col0, AccT& acc, const GemmArgs& a,
+                                              const Refill& rf) {
     constexpr int BK = Cfg::BK, TM = Cfg::TM, TN = Cfg::TN, AK = Cfg::AK;
+    constexpr int STEPS = BK / AK;
+    constexpr int P = Cfg::SPREAD;
+    static_assert(P == 0 || (STEPS % P == 0), "parts at evenly spaced steps");
+    constexpr int SPAN = P > 0 ? STEPS / P : 1;   // AK-steps between two parts
     if constexpr (Cfg::PIPE) {
         // Two fragment sets: the loads for the next step are issued before the
         // current step's FMAs, so shared-memory latency hides behind them.
@@ -369,6 +430,9 @@ __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, 
         load_b_frag<Cfg>(sB, b_col0, 0, b[0]);
 #pragma unroll
         for (int kq = 0; kq < BK; kq += AK) {
+            if constexpr (P > 0) {
+                if ((kq / AK) % SPAN == 0 && rf.on) refill_part<Cfg, P>(a, rf, (kq / AK) / SPAN);
+            }
             const int ab = (kq / AK) & 1;
             if (kq + AK < BK) load_a_frag<Cfg>(sA, a_row0, kq + AK, av[ab ^ 1]);
 #pragma unroll
@@ -382,18 +446,30 @@ __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, 
             }
         }
     } else {
-#pragma unroll Cfg::KU
-        for (int kq = 0; kq < BK; kq += AK) {
-            float av[TM][AK];
-            load_a_frag<Cfg>(sA, a_row0, kq, av);
+        // Loop bodies of KU AK-steps.
+        constexpr int H = BK / (Cfg::KU * AK);
+        static_assert(BK % (Cfg::KU * AK) == 0, "KU steps divide the slice");
+        static_assert(P == 0 || Cfg::KU % SPAN == 0, "parts at the same steps of every body");
+#pragma unroll 1
+        for (int h = 0; h < H; ++h) {
 #pragma unroll
-            for (int kk = 0; kk < AK; ++kk) {
-                float4 b[TN / 4];
-                load_b_frag<Cfg>(sB, b_col0, kq + kk, b);
-                float ak[TM];
+            for (int s = 0; s < Cfg::KU; ++s) {
+                if constexpr (P > 0) {
+                    if (s % SPAN == 0 && rf.on)
+                        refill_part<Cfg, P>(a, rf, h * (Cfg::KU / SPAN) + s / SPAN);
+                }
+                const int kq = (h * Cfg::KU + s) * AK;
+                float av[TM][AK];
+                load_a_frag<Cfg>(sA, a_row0, kq, av);
 #pragma unroll
-                for (int i = 0; i < TM; ++i) ak[i] = av[i][kk];
-                acc.rank1(ak, b);
+                for (int kk = 0; kk < AK; ++kk) {
+                    float4 b[TN / 4];
+                    load_b_frag<Cfg>(sB, b_col0, kq + kk, b);
+                    float ak[TM];
+#pragma unroll
+                    for (int i = 0; i < TM; ++i) ak[i] = av[i][kk];
+                    acc.rank1(ak, b);
+                }
             }
         }
     }
@@ -595,19 +671,38 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MINB) sgemm_ffma_kernel(const Ge
     for (long long c = 0; c < w.total; ++c) {
         cp_async_wait<STAGES - 2>();
         __syncthreads();
-        // Refill the slot computed in the previous iteration.
+        // Refill the slot computed in the previous iteration: in one burst here, or
+        // spread over the first loop body of this slice's compute (SPREAD).
+        Refill rf;
+        rf.on = false;
         if (ld.c < w.total) {
             const int ls = (stage + STAGES - 1) % STAGES;
+            float* const la = sA0 + ls * Cfg::A_STAGE;
+            float* const lb = sB0 + ls * Cfg::B_STAGE;
             int m0, n0;
             tile_origin(a, ld.tile, Cfg::BM, Cfg::BN, m0, n0);
-            load_slice<Cfg>(a, sA0 + ls * Cfg::A_STAGE, sB0 + ls * Cfg::B_STAGE, m0, n0,
-                            ld.kt * BK, tid);
+            const int k0 = ld.kt * BK;
             ld.advance(w);
+            if constexpr (Cfg::SPREAD > 0) {
+                using IC = InteriorCopy<Cfg>;
+                static_assert(IC::OK, "spread refills need the 16-byte interior copy layout");
+                rf.on = m0 + Cfg::BM <= a.M && n0 + Cfg::BN <= a.N && k0 + BK <= a.K;
+                if (rf.on) {
+                    const int ra = tid / IC::CPR, ca = (tid % IC::CPR) * 4;
+                    const int rb = tid / IC::CPRB, cb = (tid % IC::CPRB) * 4;
+                    rf.sa = smem_addr(la + ra * Cfg::LDAS + ca);
+                    rf.sb = smem_addr(lb + rb * Cfg::LDBS + cb);
+                    rf.ga = a.A + static_cast<long long>(m0 + ra) * a.lda + (k0 + ca);
+                    rf.gb = a.B + static_cast<long long>(k0 + rb) * a.ldb + (n0 + cb);
+                }
+            }
+            // Edge slices (and SPREAD = 0): the whole slice now, bounds checked.
+            if (!rf.on) load_slice<Cfg>(a, la, lb, m0, n0, k0, tid);
         }
-        cp_async_commit();
 
         compute_slice<Cfg>(sA0 + stage * Cfg::A_STAGE, sB0 + stage * Cfg::B_STAGE, a_row0,
-                           b_col0, acc);
+                           b_col0, acc, a, rf);
+        cp_async_commit();
         stage = (stage + 1 == STAGES) ? 0 : stage + 1;
 
         if (cp.kt + 1 == cp.kt_end) {

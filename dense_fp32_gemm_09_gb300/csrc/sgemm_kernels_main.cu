@@ -4,24 +4,25 @@
 
 namespace sgemm {
 
-// FfmaCfg<BM, BN, BK, TM, TN, LR, WARPS_M, WARPS_N, STAGES, VEC, AK, FMA2, MINB, PIPE, KU>
+// FfmaCfg<BM, BN, BK, TM, TN, LR, WARPS_M, WARPS_N, STAGES, VEC, AK, FMA2, MINB, PIPE, KU,
+//         SPREAD>
 // One 256-thread CTA per SM with 8 x 16 register tiles (up to 255 registers): the
 // large-problem workhorses; BK = 64 halves the per-slice overhead when K is long.
-// The 128 x 256 x 64 one double-buffers its fragments (A two k at a time): 1.2 %
-// faster at 2048^3 .. 8192^3 than single-buffered fragments four k at a time.
-// The 256 x 128 x 64 one, the same eight 32 x 128 warp tiles stacked along M and
-// fragments single-buffered, is 0.7 % faster still at those sizes (double-
-// buffering it measured slower).  Its slice loop is unrolled over half a slice (8
-// steps of 4 k) rather than all of it: 0.6-3.1 % faster at 8192^3 .. 2048^3 than
-// the full unroll, whose body is too large for the instruction caches.  It serves
-// aligned problems with K >= 2048, and
-// its 32-deep, 4-stage twin those with K < 2048 (2.7-4 % faster than the TMA-fed
-// 128 x 256 x 32 entry at 1536^3 .. 3008 x 2048 x 2000, equal at 1024^3).
-using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 2, true, 1, true>;
-using W256K32 = FfmaCfg<128, 256, 32, 8, 16, 4, 4, 2, 4, 4, 4, true, 1>;
+// SPREAD issues the next slice's copies of an interior tile in that many parts
+// spaced over the current slice instead of one burst (sgemm_ffma.cuh,
+// compute_slice); same box, interleaved, against one burst:
+//   * 128 x 256 x 64, fragments double-buffered (A two k at a time), 4 parts:
+//     4096^3 61.4 -> 65.4 TFLOP/s, 8192^3 62.3 -> 66.5;
+//   * 256 x 128 x 64, the eight 32 x 128 warp tiles stacked along M, slice loop
+//     unrolled over half a slice, 8 parts: 4096^3 61.9 -> 64.1, 2048^3 57.3 ->
+//     59.4 (where the double-buffered entry reaches 58.5);
+//   * 128 x 256 x 32 and 256 x 128 x 32, 4 stages, 8 parts: 1536^3 51.1 (256 x 128,
+//     one burst) -> 53.4 and 52.6; 1024^3 unchanged.
+using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 2, true, 1, true, 0, 4>;
+using W256K32 = FfmaCfg<128, 256, 32, 8, 16, 4, 4, 2, 4, 4, 4, true, 1, false, 0, 8>;
 using W256K16 = FfmaCfg<128, 256, 16, 8, 16, 4, 4, 2, 6, 4, 4, true, 1>;
-using H256K64 = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1, false, 8>;
-using H256K32 = FfmaCfg<256, 128, 32, 8, 16, 4, 8, 1, 4, 4, 4, true, 1>;
+using H256K64 = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1, false, 8, 8>;
+using H256K32 = FfmaCfg<256, 128, 32, 8, 16, 4, 8, 1, 4, 4, 4, true, 1, false, 0, 8>;
 // Two CTAs per SM with 8 x 8 tiles (128 registers).
 using S128K32 = FfmaCfg<128, 128, 32, 8, 8, 4, 4, 2, 3, 4, 4, true, 2>;
 // Scalar-FFMA counterpart of the same tile, kept for comparison with fma.rn.f32x2.

@@ -441,9 +441,10 @@ def test_query_config_matches_bench_choice(cuda):
     (2048, 64, 4096, "64x64x16_t8x8_s3_f2_v4"),
     (8192, 128, 4096, "256x128x64_t8x16_s2_f2_v4"),
     (8192, 96, 4096, "256x128x64_t8x16_s2_f2_v4"),
-    (4096, 4096, 4096, "256x128x64_t8x16_s2_f2_v4"),
-    (1024, 1024, 1024, "256x128x32_t8x16_s4_f2_v4"),
-    (1536, 1536, 1536, "256x128x32_t8x16_s4_f2_v4"),
+    (4096, 4096, 4096, "128x256x64_t8x16_s2_f2_v4"),
+    (2048, 2048, 2048, "256x128x64_t8x16_s2_f2_v4"),
+    (1024, 1024, 1024, "128x256x32_t8x16_s4_f2_v4"),
+    (1536, 1536, 1536, "128x256x32_t8x16_s4_f2_v4"),
     (256, 256, 256, "32x32x16_t4x4_s3_f2_v4"),
     (384, 384, 384, "32x32x16_t4x4_s3_f2_v4"),
     (512, 512, 512, "64x64x16_t8x8_s3_f2_v4"),
@@ -453,8 +454,9 @@ def test_query_config_matches_bench_choice(cuda):
 def test_narrow_c_tile_choice(cuda, M, N, K, name):
     """Narrow C gets tiles no wider than it: 512 x 64 for N <= 64 once M fills eight
     of them, 256 x 128 for N <= 128.  Square-ish C takes 64-deep slices when K >= 2048
-    or every CTA gets about 20 of them, 32-deep ones below; the smallest problems take
-    32 x 32 tiles."""
+    or every CTA gets about 20 of them (128 x 256 tiles with double-buffered fragments
+    once K >= 2048 and they fill two waves), 32-deep ones on 128 x 256 tiles below;
+    the smallest problems take 32 x 32 tiles."""
     assert sgemm_query_config(M, N, K)["name"] == name
 
 

@@ -20,16 +20,22 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
 
 
 @pytest.mark.parametrize("shape,expected", [
-    # Square and large: 64-deep slices once K >= 2048 ...
-    ((4096, 4096, 4096), "256x128x64_t8x16_s2_f2_v4"),
-    ((2048, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),
-    ((8192, 8192, 8192), "256x128x64_t8x16_s2_f2_v4"),
+    # Square and large: 64-deep slices once K >= 2048; double-buffered fragments on
+    # 128 x 256 tiles when those fill two waves (4096^3: 32*16 = 512 >= 2*152) ...
+    ((4096, 4096, 4096), "128x256x64_t8x16_s2_f2_v4"),
+    ((8192, 8192, 8192), "128x256x64_t8x16_s2_f2_v4"),
+    ((4864, 4864, 2048), "128x256x64_t8x16_s2_f2_v4"),  # 38*19 = 722 tiles
+    ((2048, 4864, 2048), "128x256x64_t8x16_s2_f2_v4"),  # 16*19 = 304: two waves exactly
+    ((1920, 4864, 2048), "256x128x64_t8x16_s2_f2_v4"),  # 15*19 = 285 < 304
+    ((2048, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),  # 16*8 = 128 < 304
+    ((4096, 4096, 2044), "256x128x64_t8x16_s2_f2_v4"),  # K below 2048
     # ... or once every CTA gets about 20 of them (16*32*24 = 12288 >= 20*152) ...
     ((4096, 4096, 1536), "256x128x64_t8x16_s2_f2_v4"),
-    # ... else 32-deep slices (1024^3: 4*8*16 = 512 64-deep slices; 1536^3: 1728).
-    ((1024, 1024, 1024), "256x128x32_t8x16_s4_f2_v4"),
-    ((1536, 1536, 1536), "256x128x32_t8x16_s4_f2_v4"),
-    ((1024, 2048, 2044), "256x128x32_t8x16_s4_f2_v4"),  # 4*16*32 = 2048 < 20*152
+    # ... else 32-deep slices on 128 x 256 tiles (1024^3: 4*8*16 = 512 64-deep
+    # slices; 1536^3: 1728).
+    ((1024, 1024, 1024), "128x256x32_t8x16_s4_f2_v4"),
+    ((1536, 1536, 1536), "128x256x32_t8x16_s4_f2_v4"),
+    ((1024, 2048, 2044), "128x256x32_t8x16_s4_f2_v4"),  # 4*16*32 = 2048 < 20*152
     ((1536, 2048, 2044), "256x128x64_t8x16_s2_f2_v4"),  # 6*16*32 = 3072 >= 20*152
     # The smallest problems: at most SMs/4 tiles of 64 x 64 and K <= 1024.
     ((256, 256, 256), "32x32x16_t4x4_s3_f2_v4"),
@@ -49,7 +55,7 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     # Below M = 4096 that rule yields: 32 tiles of 128^2 are fewer than SMs/4.
     ((4095, 128, 1024), "64x64x16_t8x8_s3_f2_v4"),
     ((2048, 256, 1024), "64x64x16_t8x8_s3_f2_v4"),     # 32 tiles of 128^2
-    ((4096, 256, 1024), "256x128x32_t8x16_s4_f2_v4"),  # 64 tiles of 128^2: 256 > 152
+    ((4096, 256, 1024), "128x256x32_t8x16_s4_f2_v4"),  # 64 tiles of 128^2: 256 > 152
 ])
 def test_rules_for_aligned_operands(lib, shape, expected):
     assert _choose(lib, *shape) == (expected, 0)
@@ -58,7 +64,9 @@ def test_rules_for_aligned_operands(lib, shape, expected):
 def test_sm_count_moves_the_thresholds(lib):
     # 13 SMs: 1024^3 has 512 >= 20*13 deep slices; 256^3 is no longer "few tiles".
     assert _choose(lib, 1024, 1024, 1024, sms=13)[0] == "256x128x64_t8x16_s2_f2_v4"
-    assert _choose(lib, 256, 256, 256, sms=13)[0] == "256x128x32_t8x16_s4_f2_v4"
+    assert _choose(lib, 256, 256, 256, sms=13)[0] == "128x256x32_t8x16_s4_f2_v4"
+    # 13 SMs: 2048^3 has 128 tiles of 128 x 256, more than two waves of 13.
+    assert _choose(lib, 2048, 2048, 2048, sms=13)[0] == "128x256x64_t8x16_s2_f2_v4"
     # Many SMs: 1024^3 has 256 tiles of 64^2, within SMs/4 at 1024 SMs.
     assert _choose(lib, 1024, 1024, 1024, sms=1024)[0] == "32x32x16_t4x4_s3_f2_v4"
     assert _choose(lib, 1024, 1024, 1024, sms=1023)[0] == "64x64x16_t8x8_s3_f2_v4"
@@ -75,12 +83,12 @@ def test_misaligned_operands_small_products_take_scalar_loads(lib):
 
 def test_misaligned_operands_large_products_are_packed(lib):
     # 1291^3 >= 2^31: the misaligned operand alone is packed, then the aligned rules apply.
-    assert _choose(lib, 1291, 1292, 1292, lda=1293) == ("256x128x32_t8x16_s4_f2_v4", 1)
-    assert _choose(lib, 1292, 1292, 1292, b_off=1) == ("256x128x32_t8x16_s4_f2_v4", 2)
+    assert _choose(lib, 1291, 1292, 1292, lda=1293) == ("128x256x32_t8x16_s4_f2_v4", 1)
+    assert _choose(lib, 1292, 1292, 1292, b_off=1) == ("128x256x32_t8x16_s4_f2_v4", 2)
     assert _choose(lib, 1290, 1292, 1288, lda=1289)[1] == 0     # 1290*1292*1288 < 2^31
     # The ragged workload: odd leading dimensions everywhere, both packed.
     assert _choose(lib, 3001, 2047, 1999, lda=2001, ldb=2049) == ("256x128x64_t8x16_s2_f2_v4", 3)
-    assert _choose(lib, 4096, 4096, 4096, a_off=3, b_off=1) == ("256x128x64_t8x16_s2_f2_v4", 3)
+    assert _choose(lib, 4096, 4096, 4096, a_off=3, b_off=1) == ("128x256x64_t8x16_s2_f2_v4", 3)
 
 
 def test_chosen_entry_matches_operand_alignment(lib):
@@ -100,7 +108,7 @@ def test_chosen_entry_matches_operand_alignment(lib):
 
 def test_forced_kernel_variable_is_not_consulted(lib, monkeypatch):
     monkeypatch.setenv("SGEMM_FORCE_KERNEL", "64x64x16_t4x4_s3_f1_v4")
-    assert _choose(lib, 4096, 4096, 4096)[0] == "256x128x64_t8x16_s2_f2_v4"
+    assert _choose(lib, 4096, 4096, 4096)[0] == "128x256x64_t8x16_s2_f2_v4"
 
 
 def test_invalid_arguments(lib):
