@@ -40,9 +40,10 @@ def describe(w) -> str:
     return f"{w.name}: M={w.M} N={w.N} K={w.K} fp32 row-major, A,B ~ {dist} seed {w.seed}"
 
 
-# Files whose text is the code of the FFMA kernels (the tile-table entry name
-# encodes the template parameters).
-KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_args.h", "sgemm_epilogue.cuh"]
+# Files whose text is the code of the FFMA kernels, the tile table's template
+# parameters included.
+KERNEL_SOURCES = ["sgemm_ffma.cuh", "sgemm_sched.cuh", "sgemm_args.h", "sgemm_epilogue.cuh",
+                  "sgemm_kernels_main.cu", "sgemm_kernels_small.cu", "sgemm_kernels_any.cu"]
 
 
 def code_only(text: str) -> str:
