@@ -307,7 +307,7 @@ def bench_gpu(args, w, dist_ctx):
         run_args = (w.M, w.N, w.K, dA.data_ptr(), w.K, dB.data_ptr(), w.N, dC.data_ptr(), w.N,
                     sh)
     if kid is not None:
-        cfg = {k: None for k in ("grid", "tiles", "sk_tiles", "ctas_per_sm")}
+        cfg = {k: None for k in ("grid", "tiles", "sk_tiles", "ctas_per_sm", "cluster")}
         cfg["name"] = sg.kernel_table()[kid]["name"]
     elif ta or tb:   # the product runs on 16-byte-aligned transposed copies
         cfg = sg.sgemm_query_config(w.M, w.N, w.K, (w.K + 3) // 4 * 4, (w.N + 3) // 4 * 4, w.N,
@@ -401,9 +401,9 @@ def bench_line(args, w, world, med_ms, mean_ms, t_wall, e2e_ms, clocks, cfg, lau
             w, world, (f"; C = {args.alpha:g}*A.B + {args.beta:g}*C" if scaled else "")
             + (f"; operands {args.trans} (T = stored transposed, transposed on the device "
                f"inside the step)" if trans else "")),
-        "plan": {"kernel": cfg["name"], "grid": cfg["grid"], "tiles": cfg["tiles"],
-                 "sk_tiles": cfg["sk_tiles"], "cluster": cfg["cluster"],
-                 "ctas_per_sm": cfg["ctas_per_sm"]},
+        "plan": {"kernel": cfg["name"], "grid": cfg.get("grid"), "tiles": cfg.get("tiles"),
+                 "sk_tiles": cfg.get("sk_tiles"), "cluster": cfg.get("cluster"),
+                 "ctas_per_sm": cfg.get("ctas_per_sm")},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak_tflops,
                      "unit": "TFLOP/s", "frac": achieved / peak_tflops,
                      "traffic": None if trans else recorded_traffic(cfg["name"], w.name),

@@ -25,13 +25,19 @@
 //     in 16-byte units puts the LR rows a warp reads in distinct banks.  The B
 //     slice is unpadded; each LDS.128 of a warp touches LC consecutive 16-byte
 //     chunks of one row.  (The pages' `+PADK/+PADN` padding, GE_v2 page §2.)
+//   * The copies of the next slice of an interior tile go out in parts spread
+//     over the current slice's k-steps (SPREAD), not in one burst before it: data
+//     landing in shared memory all at once holds up the fragment loads.
 //   * The grid is persistent (SM count x resident CTAs).  Each CTA walks a flat
 //     list of k-slices that may cross tile boundaries, so the copy pipeline
 //     never drains between tiles.  Whole waves of tiles are data-parallel; the
 //     last partial wave is shared out by k-slices over all CTAs (stream-K).  Each
 //     CTA writes its partial tiles to a workspace and a second, bandwidth-bound
-//     kernel (sgemm_reduce.cuh) sums every split tile's partials over all SMs in
+//     kernel (sgemm_reduce.cu) sums every split tile's partials over all SMs in
 //     a fixed order, so results are identical from run to run.
+//   * Problems of less than one resident wave may instead split every tile over
+//     a thread-block cluster whose CTAs sum their partial tiles in distributed
+//     shared memory, in k order, inside the same launch (cluster_sum_store).
 #pragma once
 
 #include <stdint.h>
