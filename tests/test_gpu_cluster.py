@@ -125,3 +125,31 @@ def test_small_cube_takes_one_launch(cuda, oracle_mod):
     torch.cuda.synchronize()
     ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
     assert np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref)) <= tolerance(A, B)
+
+
+def test_chained_cluster_products_see_their_inputs_complete(cuda, oracle_mod):
+    """Products on one stream, each reading the C of the one before, alternating
+    cluster splits (one launch, programmatic dependent of the previous kernel) with
+    a stream-K product (main kernel + reduction): every stage must see its inputs
+    complete."""
+    torch = cuda
+    g = torch.Generator().manual_seed(22)
+
+    def u(r, c):
+        return ((torch.rand(r, c, generator=g) - 0.5) * 0.2).cuda()
+
+    X0, B1, B2, B3, B4 = u(256, 256), u(256, 256), u(256, 768), u(768, 4096), u(4096, 384)
+    shapes = [(256, 256, 256), (256, 768, 256), (256, 4096, 768), (256, 384, 4096)]
+    plans = [sgemm_query_config(*s) for s in shapes]
+    assert all(plans[i]["cluster"] >= 2 for i in (0, 1, 3)), plans
+    assert plans[2]["cluster"] == 0 and plans[2]["sk_tiles"] > 0, plans[2]
+    C1 = sgemm(X0, B1)
+    C2 = sgemm(C1, B2)
+    C3 = sgemm(C2, B3)
+    C4 = sgemm(C3, B4)
+    torch.cuda.synchronize()
+    for A, B, C in ((X0, B1, C1), (C1, B2, C2), (C2, B3, C3), (C3, B4, C4)):
+        a, b = A.cpu(), B.cpu()
+        ref = oracle_mod.gemm_f64(a.numpy(), b.numpy())
+        err = np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref))
+        assert err <= tolerance(a, b), (tuple(A.shape), tuple(B.shape), err)

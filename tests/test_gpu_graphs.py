@@ -1,8 +1,9 @@
 """The product inside a captured CUDA graph: replays recompute C from whatever
 the captured input buffers hold.  Captured launches include the stream-K
-reduction (a programmatic dependent launch) and, for the TMA entry, tensor maps
-passed by value; the library's workspace for the capturing stream is allocated
-by a warm-up call before capture, as the header asks."""
+reduction (a programmatic dependent launch), cluster-split launches (a cluster
+dimension launch attribute) and, for the TMA entry, tensor maps passed by value;
+the library's workspace for the capturing stream is allocated by a warm-up call
+before capture, as the header asks."""
 import numpy as np
 import pytest
 
@@ -16,8 +17,11 @@ def tol(A, B):
     return 1e-6 * A.shape[1] * float(A.abs().max()) * float(B.abs().max())
 
 
-@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (2048, 1536, 4096), (3001, 2047, 1999)])
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 1024), (2048, 1536, 4096), (3001, 2047, 1999),
+                                   (256, 256, 256), (768, 768, 768)])
 def test_graph_replay_recomputes(cuda, oracle_mod, M, N, K):
+    """1024^3 and up take stream-K (reduction launch); 256^3 and 768^3 a cluster split
+    (cluster launch attribute, one launch)."""
     torch = cuda
     A1, B = random_pair(M, N, K, seed=30)
     A2, _ = random_pair(M, N, K, seed=31)
