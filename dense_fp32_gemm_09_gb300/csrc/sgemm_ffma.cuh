@@ -232,7 +232,7 @@ struct Acc<TM, TN, true, BOUTER> {
 // ----------------------------------------------------------------------------
 template <int BM_, int BN_, int BK_, int TM_, int TN_, int LR_, int WARPS_M_, int WARPS_N_,
           int STAGES_, int VEC_, int AK_, bool FMA2_, int MINB_, bool PIPE_ = false,
-          int KU_ = 0, int SPREAD_ = 0>
+          int KU_ = 0, int SPREAD_ = 0, int SPREAD_FRAC_ = 1>
 struct FfmaCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_, TM = TM_, TN = TN_;
     static constexpr int LR = LR_, LC = 32 / LR_;
@@ -251,6 +251,8 @@ struct FfmaCfg {
     // issued at evenly spaced AK-steps of the first loop body of compute_slice,
     // instead of one burst before it (see compute_slice).
     static constexpr int SPREAD = SPREAD_;
+    // The parts go into the first 1 / SPREAD_FRAC of the slice's k-steps.
+    static constexpr int SPREAD_FRAC = SPREAD_FRAC_;
     // A slice: [BM][BK + PADA] (row stride odd in 16-byte units); B slice: [BK][BN].
     static constexpr int PADA = ((BK / 4) % 2 == 0) ? 4 : 0;
     static constexpr int LDAS = BK + PADA;
@@ -423,7 +425,7 @@ __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, 
                                               int b_col0, AccT& acc, const GemmArgs& a,
                                               const Refill& rf) {
     constexpr int BK = Cfg::BK, TM = Cfg::TM, TN = Cfg::TN, AK = Cfg::AK;
-    constexpr int STEPS = BK / AK;
+    constexpr int STEPS = BK / AK / Cfg::SPREAD_FRAC;   // k-steps the parts spread over
     constexpr int P = Cfg::SPREAD;
     static_assert(P == 0 || (STEPS % P == 0), "parts at evenly spaced steps");
     constexpr int SPAN = P > 0 ? STEPS / P : 1;   // AK-steps between two parts
@@ -437,7 +439,8 @@ __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, 
 #pragma unroll
         for (int kq = 0; kq < BK; kq += AK) {
             if constexpr (P > 0) {
-                if ((kq / AK) % SPAN == 0 && rf.on) refill_part<Cfg, P>(a, rf, (kq / AK) / SPAN);
+                if ((kq / AK) % SPAN == 0 && (kq / AK) / SPAN < P && rf.on)
+                    refill_part<Cfg, P>(a, rf, (kq / AK) / SPAN);
             }
             const int ab = (kq / AK) & 1;
             if (kq + AK < BK) load_a_frag<Cfg>(sA, a_row0, kq + AK, av[ab ^ 1]);
@@ -461,8 +464,9 @@ __device__ __forceinline__ void compute_slice(const float* sA, const float* sB, 
 #pragma unroll
             for (int s = 0; s < Cfg::KU; ++s) {
                 if constexpr (P > 0) {
-                    if (s % SPAN == 0 && rf.on)
-                        refill_part<Cfg, P>(a, rf, h * (Cfg::KU / SPAN) + s / SPAN);
+                    const int part = h * (Cfg::KU / SPAN) + s / SPAN;
+                    if (s % SPAN == 0 && (Cfg::SPREAD_FRAC == 1 || part < P) && rf.on)
+                        refill_part<Cfg, P>(a, rf, part);
                 }
                 const int kq = (h * Cfg::KU + s) * AK;
                 float av[TM][AK];

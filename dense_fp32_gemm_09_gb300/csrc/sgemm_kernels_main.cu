@@ -5,23 +5,26 @@
 namespace sgemm {
 
 // FfmaCfg<BM, BN, BK, TM, TN, LR, WARPS_M, WARPS_N, STAGES, VEC, AK, FMA2, MINB, PIPE, KU,
-//         SPREAD>
+//         SPREAD, SPREAD_FRAC>
 // One 256-thread CTA per SM with 8 x 16 register tiles (up to 255 registers): the
 // large-problem workhorses; BK = 64 halves the per-slice overhead when K is long.
-// SPREAD issues the next slice's copies of an interior tile in that many parts
-// spaced over the current slice instead of one burst (sgemm_ffma.cuh,
-// compute_slice); same box, interleaved, against one burst:
-//   * 128 x 256 x 64, fragments double-buffered (A two k at a time), 4 parts:
-//     4096^3 61.4 -> 65.4 TFLOP/s, 8192^3 62.3 -> 66.5;
+// SPREAD issues the next slice's copies of an interior tile in that many parts at
+// evenly spaced k-steps of the first 1 / SPREAD_FRAC of the current slice, instead
+// of one burst before it (sgemm_ffma.cuh, compute_slice).  Same box, interleaved
+// (TFLOP/s at 4096^3 / 8192^3 / 2048^3):
+//   * 128 x 256 x 64, fragments double-buffered (A two k at a time): one burst
+//     61.4 / 62.3 / 55.5; 4 parts over the whole slice 65.3 / 66.4 / 58.5; over
+//     its first half 65.1 / 66.2; over its first quarter (every 4 k) 66.0 / 67.2 /
+//     58.9; 8 parts over a quarter 64.9 / 66.1; 2 parts 63.8-64.3;
 //   * 256 x 128 x 64, the eight 32 x 128 warp tiles stacked along M, slice loop
-//     unrolled over half a slice, 8 parts: 4096^3 61.9 -> 64.1, 2048^3 57.3 ->
-//     59.4 (where the double-buffered entry reaches 58.5);
-//   * 128 x 256 x 32 and 256 x 128 x 32, 4 stages, 8 parts: 1536^3 51.1 (256 x 128,
-//     one burst) -> 53.4 and 52.6; 1024^3 unchanged.
-using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 2, true, 1, true, 0, 4>;
+//     unrolled over half a slice: one burst 61.9 / 62.6 / 57.3; 8 parts over the
+//     slice 64.0 / 64.8 / 59.4; 4 over its first half 64.5 / 65.2 / 59.5;
+//   * 128 x 256 x 32 and 256 x 128 x 32, 4 stages, 8 parts over the slice: 1536^3
+//     51.1 (256 x 128, one burst) -> 53.4 and 52.6; 1024^3 unchanged.
+using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 2, true, 1, true, 0, 4, 4>;
 using W256K32 = FfmaCfg<128, 256, 32, 8, 16, 4, 4, 2, 4, 4, 4, true, 1, false, 0, 8>;
 using W256K16 = FfmaCfg<128, 256, 16, 8, 16, 4, 4, 2, 6, 4, 4, true, 1>;
-using H256K64 = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1, false, 8, 8>;
+using H256K64 = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1, false, 8, 4, 2>;
 using H256K32 = FfmaCfg<256, 128, 32, 8, 16, 4, 8, 1, 4, 4, 4, true, 1, false, 0, 8>;
 // Two CTAs per SM with 8 x 8 tiles (128 registers).
 using S128K32 = FfmaCfg<128, 128, 32, 8, 8, 4, 4, 2, 3, 4, 4, true, 2>;
