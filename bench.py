@@ -552,6 +552,68 @@ def bench_tf32x3(args, w, dist_ctx):
     }
 
 
+def bench_link(args):
+    """Host<->device copy bandwidth from pinned host memory (the bound of the e2e
+    lines): each direction alone, both at once, and one copy cut into 4 pieces on 4
+    streams.  CUDA events around each copy, median of the steps."""
+    import torch
+    dev = torch.device("cuda", 0)
+    out = []
+    for mb in (16, 64, 256):
+        n = (mb << 20) // 4
+        h_in = torch.empty(n, dtype=torch.float32).pin_memory()
+        h_out = torch.empty(n, dtype=torch.float32).pin_memory()
+        d_a = torch.empty(n, dtype=torch.float32, device=dev)
+        d_b = torch.empty(n, dtype=torch.float32, device=dev)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        split = [torch.cuda.Stream(dev) for _ in range(4)]
+
+        def timed(fn, nbytes):
+            ts = []
+            for i in range(args.warmup + args.steps):
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                e1.synchronize()
+                if i >= args.warmup:
+                    ts.append(e0.elapsed_time(e1))
+            ms = statistics.median(ts)
+            return {"ms": ms, "gb_s": nbytes / (ms * 1e-3) / 1e9}
+
+        def both():
+            cur = torch.cuda.current_stream(dev)
+            for st in (s_in, s_out):
+                st.wait_stream(cur)
+            with torch.cuda.stream(s_in):
+                d_a.copy_(h_in, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                h_out.copy_(d_b, non_blocking=True)
+            cur.wait_stream(s_in)
+            cur.wait_stream(s_out)
+
+        def four():
+            cur = torch.cuda.current_stream(dev)
+            q = n // 4
+            for j, st in enumerate(split):
+                st.wait_stream(cur)
+                with torch.cuda.stream(st):
+                    d_a[j * q:(j + 1) * q].copy_(h_in[j * q:(j + 1) * q], non_blocking=True)
+            for st in split:
+                cur.wait_stream(st)
+
+        row = {"bytes": 4 * n,
+               "h2d": timed(lambda: d_a.copy_(h_in, non_blocking=True), 4 * n),
+               "d2h": timed(lambda: h_out.copy_(d_b, non_blocking=True), 4 * n),
+               "both_directions": timed(both, 8 * n),
+               "h2d_4_streams": timed(four, 4 * n)}
+        out.append(row)
+        print(json.dumps({"metric": "host<->device copy bandwidth, pinned host memory",
+                          "unit": "GB/s", **row}), flush=True)
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,9 +633,15 @@ def main(argv=None):
     ap.add_argument("--tile-sweep", action="store_true",
                     help="one line per tile-table entry that can serve the workload "
                          "(forced entry, no e2e or CPU baseline)")
+    ap.add_argument("--link", action="store_true",
+                    help="host<->device copy bandwidth from pinned memory (what bounds "
+                         "the e2e lines); no product")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.link:
+        bench_link(args)
+        return 0
 
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
