@@ -427,6 +427,52 @@ def bench_line(args, w, world, med_ms, mean_ms, t_wall, e2e_ms, clocks, cfg, lau
 TF32_PER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor rates of the GB300
 
 
+def tf32x3_summary(args, w, ctx) -> dict:
+    """The 3xTF32 tensor-core variant on the same workload, measured in the same run and
+    reported beside (never instead of) the FP32 line: its own value and roofline."""
+    import argparse
+    try:
+        sub = argparse.Namespace(**{**vars(args), "steps": min(args.steps, 10),
+                                    "warmup": max(3, min(args.warmup, 5))})
+        line = bench_tf32x3(sub, w, ctx)
+        if line is None:
+            return {"error": "not rank 0"}
+        keep = ("value", "unit", "ms_per_step", "ms_split", "ms_gemm", "dtype", "roofline",
+                "clocks", "gpu_launches")
+        return {k: line[k] for k in keep if k in line}
+    except Exception as exc:   # noqa: BLE001 - the FP32 line stands on its own
+        return {"error": f"{type(exc).__name__}: {exc}"[:300]}
+
+
+def measured_tf32_peak(dev, n: int = 8192, reps: int = 5):
+    """Dense TF32 tensor rate measured here, as the driver measures bf16: cuBLAS
+    through torch.matmul on fp32 n^3 operands with TF32 allowed, best of `reps` after
+    a warm-up (context only: nothing on the product path calls it).  None if it fails."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    try:
+        torch.backends.cuda.matmul.allow_tf32 = True
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(2):
+            torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:   # noqa: BLE001 - a context figure, never the product
+        return None
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def bench_tf32x3(args, w, dist_ctx):
     """The 3xTF32 tensor-core variant: one step = one sgemm_tf32x3_run_ex call
     (operand split + tcgen05 GEMM), inputs resident.  The split and the GEMM are
@@ -524,7 +570,15 @@ def bench_tf32x3(args, w, dist_ctx):
         return None
     peaks = measured_peaks()
     bf16 = float(peaks.get("bf16_tflops") or 1900.0)
-    peak = bf16 * TF32_PER_BF16
+    tf32 = measured_tf32_peak(dev)
+    if tf32 is not None:
+        peak = tf32
+        basis = (f"measured here: cuBLAS TF32 GEMM 8192^3 {tf32:.1f} TFLOP/s (torch.matmul, "
+                 f"TF32 allowed, best of 5); 3 TF32 MMAs per product")
+    else:
+        peak = bf16 * TF32_PER_BF16
+        basis = (f"measured bf16 {bf16:.1f} TFLOP/s x nominal TF32/BF16 ratio "
+                 f"{TF32_PER_BF16:.3f}; 3 TF32 MMAs per product")
     flops = float(w.flops)
     clk = clocks.summary()
     return {
@@ -541,8 +595,8 @@ def bench_tf32x3(args, w, dist_ctx):
         "roofline": {"bound": "tensor", "achieved": 3 * flops / (gemm_ms * 1e-3) / 1e12,
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": 3 * flops / (gemm_ms * 1e-3) / 1e12 / peak, "traffic": None,
-                     "peak_basis": f"measured bf16 {bf16:.1f} TFLOP/s x nominal TF32/BF16 "
-                                   f"ratio {TF32_PER_BF16:.3f}; 3 TF32 MMAs per product",
+                     "peak_basis": basis,
+                     "peak_derived_from_bf16": bf16 * TF32_PER_BF16,
                      "effective_fp32_tflops_gemm_only": flops / (gemm_ms * 1e-3) / 1e12},
         "clocks": clk,
         "e2e": {"value": whole_job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s",
@@ -633,6 +687,8 @@ def main(argv=None):
     ap.add_argument("--tile-sweep", action="store_true",
                     help="one line per tile-table entry that can serve the workload "
                          "(forced entry, no e2e or CPU baseline)")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="leave the 3xTF32 variant out of the default line")
     ap.add_argument("--link", action="store_true",
                     help="host<->device copy bandwidth from pinned memory (what bounds "
                          "the e2e lines); no product")
@@ -671,6 +727,11 @@ def main(argv=None):
                 cb = oracle_rate(WORKLOADS[name], A, B, target_s=12.0)
                 cb.pop("seconds", None)
                 line["cpu_baseline"] = cb
+            # (one rank only: the variant's timing uses no collective)
+            if args.path == "ffma" and not args.sweep and args.trans == "NN" and \
+                    args.alpha == 1.0 and args.beta == 0.0 and not args.no_variants and \
+                    world == 1:
+                line["variants"] = {"tf32x3": tf32x3_summary(args, WORKLOADS[name], ctx)}
             print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as tdist
