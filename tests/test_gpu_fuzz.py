@@ -2,7 +2,7 @@
 by element against the fp64 oracle (oracle_gemm_f64_op): random M, N, K, leading
 dimension padding, 4-byte misalignment of the bases, alpha/beta (including 0 and
 1) and transpose flags; C lives inside a canary-filled buffer.  The 3xTF32 path
-gets its own random cases at its own tolerance."""
+gets its own random cases at its own tolerance, and random cluster splits theirs."""
 import numpy as np
 import pytest
 
@@ -143,4 +143,42 @@ def test_random_wide_cases(cuda, oracle_mod, monkeypatch, seed):
     mask = np.ones(flat.size, dtype=bool)
     for r in range(M):
         mask[r * ldc: r * ldc + N] = False
+    assert np.all(flat[mask] == CANARY)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_cluster_split_cases(cuda, oracle_mod, monkeypatch, seed):
+    """Random shapes run as cluster splits (schedule 3, clusters of up to 2, 4 or 8
+    CTAs per tile) with random alpha/beta, leading-dimension padding and 4-byte
+    misaligned bases (the 4-byte-load entries take the cluster sum too), against the
+    oracle, with canaries around C."""
+    torch = cuda
+    lib = load()
+    rng = np.random.default_rng(4000 + seed)
+    M, N = (int(x) for x in rng.integers(1, 1500, size=2))
+    K = int(rng.integers(1, 3000))
+    alpha = float(rng.choice([1.0, -1.5, 0.25]))
+    beta = float(rng.choice([0.0, 1.0, -0.5]))
+    monkeypatch.setenv("SGEMM_CLUSTER", str(int(rng.choice([2, 4, 8]))))
+    pads = [int(x) for x in rng.integers(0, 6, size=3)]
+    offs = [int(x) for x in rng.integers(0, 2, size=3)]
+    g = torch.Generator().manual_seed(4000 + seed)
+    A = torch.rand(M, K, generator=g) * 2 - 1
+    B = torch.rand(K, N, generator=g) * 2 - 1
+    C0 = torch.rand(M, N, generator=g) * 2 - 1
+    _, dA, lda = place(torch, A, pads[0], offs[0], float("nan"))
+    _, dB, ldb = place(torch, B, pads[1], offs[1], float("nan"))
+    cbuf, dC, ldc = place(torch, C0, pads[2], offs[2], CANARY)
+    st = lib.sgemm_run_ex(M, N, K, alpha, dA.data_ptr(), lda, dB.data_ptr(), ldb, beta,
+                          dC.data_ptr(), ldc, -1, 3, torch.cuda.current_stream().cuda_stream)
+    assert st == 0, (M, N, K, lib.sgemm_last_error())
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm_f64_ex(alpha, A.numpy(), B.numpy(), beta, C0.numpy())
+    err = np.max(np.abs(dC.cpu().numpy().astype(np.float64) - ref))
+    tol = 1e-6 * (abs(alpha) * K + abs(beta)) + 1e-30
+    assert err <= tol, ((M, N, K, alpha, beta, pads, offs), err, tol)
+    flat = cbuf.cpu().numpy()
+    mask = np.ones(flat.size, dtype=bool)
+    for r in range(M):
+        mask[offs[2] + r * ldc: offs[2] + r * ldc + N] = False
     assert np.all(flat[mask] == CANARY)
