@@ -260,19 +260,23 @@ constexpr int kMaxClusterGrid = 1 << 22;
 //     pieces in clusters of 8 lost to clusters of 4 at 128^3 .. 384^3);
 //   * one resident wave (T*S <= gmax); clusters of 8 of an entry with 4 or more
 //     CTAs per SM may take up to 1.35 waves (640^3 on 64 x 64 tiles);
-//   * an entry with one CTA per SM keeps stream-K when the cluster grid would
-//     leave more than a tenth of stream-K's grid idle (1024^3 on 256 x 128
-//     tiles: 128 clustered CTAs ran 53.6 us, 152 stream-K CTAs 51.5 us).
+//   * stream-K stays when the cluster grid is well below stream-K's own grid:
+//     under 0.9 of it for an entry with one CTA per SM (1024^3 on 256 x 128
+//     tiles: 128 clustered CTAs ran 53.6 us, 152 stream-K CTAs 51.5 us), under 0.6
+//     for entries with several (2048 x 64 x 4096 on 64 x 64 tiles: 256 clustered
+//     CTAs 41.0 us, 608 stream-K CTAs 35.7; 384^3 at 0.67 and 256 x 2048 x 512 at
+//     0.84 of it still ran 9 % faster clustered).
 inline int auto_cluster_size(long long T, int KT, long long gmax, int occ, int cap) {
     long long g_sk = T * KT / kMinSkIters;   // stream-K's grid for the same tiles
     if (g_sk < T) g_sk = T;
     if (g_sk > gmax) g_sk = gmax;
+    const double keep_sk_below = occ == 1 ? 0.9 : 0.6;
     for (int S = cap; S >= 2; S /= 2) {
         const int min_slices = S >= 8 ? 4 : 2;
         if (KT < static_cast<long long>(S) * min_slices) continue;
         const double waves = (S >= 8 && occ >= 4) ? 1.35 : 1.0;
         if (static_cast<double>(T * S) > waves * static_cast<double>(gmax)) continue;
-        if (occ == 1 && static_cast<double>(T * S) < 0.9 * static_cast<double>(g_sk)) return 0;
+        if (static_cast<double>(T * S) < keep_sk_below * static_cast<double>(g_sk)) return 0;
         return S;
     }
     return 0;

@@ -279,15 +279,15 @@ def test_no_cluster_when_disabled_or_forced_otherwise(lib, monkeypatch):
 def _auto_cluster(T, KT, gmax, occ):
     """The automatic rule, restated: the largest S in 8, 4, 2 with at least 2
     slices per CTA (4 for S = 8) and one resident wave (1.35 for S = 8 when the
-    entry keeps 4 or more CTAs per SM); entries with one CTA per SM keep stream-K
-    when the cluster grid is under 0.9 of stream-K's."""
+    entry keeps 4 or more CTAs per SM); stream-K stays when the cluster grid is
+    under 0.9 (one CTA per SM) or 0.6 (several) of stream-K's grid."""
     g_sk = min(max(T * KT // 4, T), gmax)
     for S in (8, 4, 2):
         if KT < S * (4 if S == 8 else 2):
             continue
         if T * S > (1.35 if S == 8 and occ >= 4 else 1.0) * gmax:
             continue
-        if occ == 1 and T * S < 0.9 * g_sk:
+        if T * S < (0.9 if occ == 1 else 0.6) * g_sk:
             return 0
         return S
     return 0
@@ -324,6 +324,10 @@ def test_automatic_cluster_rule(lib, monkeypatch):
     (1024, 1024, 1024, "256x128x32_t8x16_s4_f2_v4", 1, 0),
     (1536, 1536, 1536, "256x128x32_t8x16_s4_f2_v4", 1, 2),
     (4096, 128, 256, "256x128x64_t8x16_s2_f2_v4", 1, 2),
+    (2048, 256, 256, "64x64x16_t8x8_s3_f2_v4", 4, 4),
+    (256, 2048, 512, "64x64x16_t8x8_s3_f2_v4", 4, 4),
+    (2048, 64, 4096, "64x64x16_t8x8_s3_f2_v4", 4, 0),
+    (1024, 64, 4096, "64x64x16_t8x8_s3_f2_v4", 4, 0),
 ])
 def test_measured_cluster_choices(lib, monkeypatch, M, N, K, name, occ, S):
     """The cluster sizes of the timed shapes on 152 SMs."""
