@@ -138,8 +138,8 @@ def test_chained_cluster_products_see_their_inputs_complete(cuda, oracle_mod):
     def u(r, c):
         return ((torch.rand(r, c, generator=g) - 0.5) * 0.2).cuda()
 
-    X0, B1, B2, B3, B4 = u(256, 256), u(256, 256), u(256, 768), u(768, 4096), u(4096, 384)
-    shapes = [(256, 256, 256), (256, 768, 256), (256, 4096, 768), (256, 384, 4096)]
+    X0, B1, B2, B3, B4 = u(256, 256), u(256, 256), u(256, 768), u(768, 4096), u(4096, 1024)
+    shapes = [(256, 256, 256), (256, 768, 256), (256, 4096, 768), (256, 1024, 4096)]
     plans = [sgemm_query_config(*s) for s in shapes]
     assert all(plans[i]["cluster"] >= 2 for i in (0, 1, 3)), plans
     assert plans[2]["cluster"] == 0 and plans[2]["sk_tiles"] > 0, plans[2]
