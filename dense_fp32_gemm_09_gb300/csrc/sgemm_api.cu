@@ -231,10 +231,14 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
         const long long slices64 =
             static_cast<long long>((M + 255) / 256) * ((N + 127) / 128) * ((K + 63) / 64);
         const long long tiles_w = static_cast<long long>((M + 127) / 128) * ((N + 255) / 256);
+        // The 256 x 128 entry spreads its refills except on tiles crossing M or N;
+        // with such tiles and under 1.5 waves its all-burst twin is faster.
+        const long long tiles_h = static_cast<long long>((M + 255) / 256) * ((N + 127) / 128);
+        const bool ragged_h = (M % 256 != 0 || N % 128 != 0) && 2 * tiles_h < 3LL * sms;
         if (K >= 2048 && tiles_w >= 2LL * sms)
             name = "128x256x64_t8x16_s2_f2_v4";
         else if (K >= 2048 || slices64 >= 20LL * sms)
-            name = "256x128x64_t8x16_s2_f2_v4";
+            name = ragged_h ? "256x128x64_t8x16_s2_f2_v4_burst" : "256x128x64_t8x16_s2_f2_v4";
         else
             name = "128x256x32_t8x16_s4_f2_v4";
     }

@@ -25,6 +25,12 @@ using W256K64 = FfmaCfg<128, 256, 64, 8, 16, 4, 4, 2, 2, 4, 2, true, 1, true, 0,
 using W256K32 = FfmaCfg<128, 256, 32, 8, 16, 4, 4, 2, 4, 4, 4, true, 1, false, 0, 8>;
 using W256K16 = FfmaCfg<128, 256, 16, 8, 16, 4, 4, 2, 6, 4, 4, true, 1>;
 using H256K64 = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1, false, 8, 4, 2>;
+// The same tile with every refill in one burst: tiles that cross M or N refill in
+// one bounds-checked burst either way, and with under 1.5 waves of tiles the CTAs
+// holding them set the pace; there the all-burst twin measured faster (3008 x 2048
+// x 2048: 57.7 against 56.4 TFLOP/s; 3004 x 2048 x 2000: 55.9 against 55.0), while
+// at 1.8 waves and more the spread one leads (2900^3: 55.9 against 55.2).
+using H256K64B = FfmaCfg<256, 128, 64, 8, 16, 4, 8, 1, 2, 4, 4, true, 1, false, 8>;
 using H256K32 = FfmaCfg<256, 128, 32, 8, 16, 4, 8, 1, 4, 4, 4, true, 1, false, 0, 8>;
 // Two CTAs per SM with 8 x 8 tiles (128 registers).
 using S128K32 = FfmaCfg<128, 128, 32, 8, 8, 4, 4, 2, 3, 4, 4, true, 2>;
@@ -36,6 +42,7 @@ static const KernelEntry kEntries[] = {
     make_entry<W256K32>("128x256x32_t8x16_s4_f2_v4"),
     make_entry<W256K16>("128x256x16_t8x16_s6_f2_v4"),
     make_entry<H256K64>("256x128x64_t8x16_s2_f2_v4"),
+    make_entry<H256K64B>("256x128x64_t8x16_s2_f2_v4_burst"),
     make_entry<H256K32>("256x128x32_t8x16_s4_f2_v4"),
     make_entry<S128K32>("128x128x32_t8x8_s3_f2_v4"),
     make_entry<S128F1>("128x128x16_t8x8_s4_f1_v4"),

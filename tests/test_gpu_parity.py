@@ -449,7 +449,7 @@ def test_query_config_matches_bench_choice(cuda):
     (384, 384, 384, "32x32x16_t4x4_s3_f2_v4"),
     (512, 512, 512, "64x64x16_t8x8_s3_f2_v4"),
     (2048, 4096, 1024, "256x128x64_t8x16_s2_f2_v4"),
-    (3008, 2048, 2000, "256x128x64_t8x16_s2_f2_v4"),
+    (3008, 2048, 2000, "256x128x64_t8x16_s2_f2_v4_burst"),
 ])
 def test_narrow_c_tile_choice(cuda, M, N, K, name):
     """Narrow C gets tiles no wider than it: 512 x 64 for N <= 64 once M fills eight

@@ -37,6 +37,12 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     ((1536, 1536, 1536), "128x256x32_t8x16_s4_f2_v4"),
     ((1024, 2048, 2044), "128x256x32_t8x16_s4_f2_v4"),  # 4*16*32 = 2048 < 20*152
     ((1536, 2048, 2044), "256x128x64_t8x16_s2_f2_v4"),  # 6*16*32 = 3072 >= 20*152
+    # Tiles crossing M or N with under 1.5 waves of 256 x 128 tiles: the all-burst twin.
+    ((3008, 2048, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # 12*16 = 192 < 228
+    ((3500, 2048, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # 14*16 = 224
+    ((3584, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),        # no tile crosses M or N
+    ((3600, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),        # 15*16 = 240 tiles
+    ((2048, 2000, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # N edge, 8*16 tiles
     # The smallest problems: at most SMs/4 tiles of 64 x 64 and K <= 1024.
     ((256, 256, 256), "32x32x16_t4x4_s3_f2_v4"),
     ((384, 384, 384), "32x32x16_t4x4_s3_f2_v4"),
@@ -87,7 +93,8 @@ def test_misaligned_operands_large_products_are_packed(lib):
     assert _choose(lib, 1292, 1292, 1292, b_off=1) == ("128x256x32_t8x16_s4_f2_v4", 2)
     assert _choose(lib, 1290, 1292, 1288, lda=1289)[1] == 0     # 1290*1292*1288 < 2^31
     # The ragged workload: odd leading dimensions everywhere, both packed.
-    assert _choose(lib, 3001, 2047, 1999, lda=2001, ldb=2049) == ("256x128x64_t8x16_s2_f2_v4", 3)
+    assert _choose(lib, 3001, 2047, 1999, lda=2001, ldb=2049) == ("256x128x64_t8x16_s2_f2_v4_burst",
+                                                                 3)
     assert _choose(lib, 4096, 4096, 4096, a_off=3, b_off=1) == ("128x256x64_t8x16_s2_f2_v4", 3)
 
 
