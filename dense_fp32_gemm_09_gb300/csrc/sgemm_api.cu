@@ -136,6 +136,21 @@ long long span(int rows, int cols, int ld) {
     return static_cast<long long>(rows - 1) * ld + cols;
 }
 
+// Tile and slice bounds (m0 + BM, k0 + BK, ...) are 32-bit in the kernels and the
+// schedule; element offsets are 64-bit.  Dimensions up to 2^30 keep every such
+// bound far from overflow (an fp32 matrix with 2^30 rows of one column is already
+// 4 GiB), so larger ones are refused before anything is planned.
+constexpr int kMaxDim = 1 << 30;
+
+int check_dims(int M, int N, int K) {
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) {
+        std::snprintf(t_last_error, sizeof(t_last_error),
+                      "dimension above 2^30: M=%d N=%d K=%d", M, N, K);
+        return SGEMM_ERR_UNSUPPORTED;
+    }
+    return SGEMM_OK;
+}
+
 // Argument checks for C[M x N] = op(A)[M x K] . op(B)[K x N]: op(A) = A stored
 // M x K (transa == 0) or A^T with A stored K x M (transa == 1); likewise B.
 int check_args_op(int transa, int transb, int M, int N, int K, const float* A, int lda,
@@ -145,6 +160,7 @@ int check_args_op(int transa, int transb, int M, int N, int K, const float* A, i
                       N, K);
         return SGEMM_ERR_INVALID_ARG;
     }
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     const int ra = transa ? K : M, ca = transa ? M : K;   // stored A: ra x ca
     const int rb = transb ? N : K, cb = transb ? K : N;   // stored B: rb x cb
     if (lda < std::max(ca, 1) || ldb < std::max(cb, 1) || ldc < std::max(N, 1)) {
@@ -797,6 +813,8 @@ int check_schedule(const Plan& p, char* why, size_t why_len) {
 
 void set_cuda_error(const char* what, cudaError_t e) { set_error(what, e); }
 
+int check_sizes(int M, int N, int K) { return check_dims(M, N, K); }
+
 int check_operands(int transa, int transb, int M, int N, int K, const float* A, int lda,
                    const float* B, int ldb, const float* C, int ldc) {
     return check_args_op(transa, transb, M, N, K, A, lda, B, ldb, C, ldc);
@@ -879,6 +897,7 @@ int sgemm_workspace_size(int M, int N, int K, int lda, int ldb, int ldc, const f
     if (M < 0 || N < 0 || K < 0 || lda < std::max(K, 1) || ldb < std::max(N, 1) ||
         ldc < std::max(N, 1))
         return SGEMM_ERR_INVALID_ARG;
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0 || K == 0) return SGEMM_OK;
     Plan p;
     const DeviceInfo* d = nullptr;
@@ -897,6 +916,7 @@ int sgemm_query_config(int M, int N, int K, int lda, int ldb, int ldc, const flo
     const float* pc = C ? C : reinterpret_cast<const float*>(uintptr_t{256} << 40);
     if (M <= 0 || N <= 0 || K <= 0 || lda < K || ldb < N || ldc < N)
         return SGEMM_ERR_INVALID_ARG;
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     Plan p;
     const DeviceInfo* d = nullptr;
     const PackPlan q = pack_plan(M, N, K, pa, lda, pb, ldb, true, -1, 0, 0);
@@ -913,6 +933,7 @@ int sgemm_schedule_check(int M, int N, int K, int kernel_id, int sms, int ctas_p
     if (M <= 0 || N <= 0 || K <= 0 || sms <= 0 || ctas_per_sm <= 0 || schedule < 0 ||
         schedule > 3 || kernel_id < 0 || kernel_id >= static_cast<int>(table().size()))
         return SGEMM_ERR_INVALID_ARG;
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     Plan p;
     p.entry = kernel_id;
     p.args.M = M; p.args.N = N; p.args.K = K;
@@ -926,6 +947,7 @@ int sgemm_choose_check(int M, int N, int K, int lda, int ldb, int a_offset, int 
     if (M <= 0 || N <= 0 || K <= 0 || lda < K || ldb < N || sms <= 0 || a_offset < 0 ||
         a_offset > 3 || b_offset < 0 || b_offset > 3 || kernel_id == nullptr)
         return SGEMM_ERR_INVALID_ARG;
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     // Stand-ins that carry only the operands' alignment.
     const float* pa = reinterpret_cast<const float*>(uintptr_t{256} + 4u * a_offset);
     const float* pb = reinterpret_cast<const float*>((uintptr_t{256} << 20) + 4u * b_offset);
@@ -937,6 +959,7 @@ int sgemm_choose_check(int M, int N, int K, int lda, int ldb, int a_offset, int 
 
 int sgemm_tf32x3_workspace_size(int M, int N, int K, size_t* out_bytes) {
     if (out_bytes == nullptr || M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_ARG;
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     *out_bytes = tf32x3_workspace_bytes(M, N, K);
     return SGEMM_OK;
 }
@@ -1012,6 +1035,7 @@ int sgemm_tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C
         std::snprintf(t_last_error, sizeof(t_last_error), "invalid argument");
         return SGEMM_ERR_INVALID_ARG;
     }
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return SGEMM_OK;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_UNSUPPORTED;
@@ -1032,6 +1056,7 @@ int sgemm_tf32x3_multiply(int M, int N, int K, float alpha, float beta, float* C
 int sgemm_tf32x3_query_config(int M, int N, int K, sgemm_config* out) {
     if (out == nullptr || M <= 0 || N <= 0 || K <= 0) return SGEMM_ERR_INVALID_ARG;
     std::memset(out, 0, sizeof(*out));
+    if (check_dims(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_UNSUPPORTED;
     const DeviceInfo* d = nullptr;

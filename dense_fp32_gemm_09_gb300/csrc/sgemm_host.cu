@@ -164,6 +164,7 @@ extern "C" {
 
 int sgemm_host_plan_check(int M, int N, int K, int* n_panels, int* rows, int* k_chunk) {
     if (M <= 0 || N <= 0 || K < 0 || n_panels == nullptr) return SGEMM_ERR_INVALID_ARG;
+    if (check_sizes(M, N, K) != SGEMM_OK) return SGEMM_ERR_UNSUPPORTED;
     int r[kMaxHostPanels];
     const int n = host_panels(M, N, K, r);
     *n_panels = n;

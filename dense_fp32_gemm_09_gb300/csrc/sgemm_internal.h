@@ -26,9 +26,13 @@ int reduce_chunks(int bm, int bn, int sk_tiles, int sms);
 void set_last_error_message(const char* msg);
 void set_cuda_error(const char* what, cudaError_t e);
 
+// SGEMM_ERR_UNSUPPORTED (with a message) when M, N or K is above 2^30, else SGEMM_OK.
+int check_sizes(int M, int N, int K);
+
 // Argument checks of the public entry points (sizes, leading dimensions of the
 // stored operands, null pointers, C overlapping A or B); op = 1 means the operand
-// is stored transposed.  SGEMM_OK or SGEMM_ERR_INVALID_ARG with a message.
+// is stored transposed.  SGEMM_OK, SGEMM_ERR_INVALID_ARG with a message, or
+// SGEMM_ERR_UNSUPPORTED for a dimension above 2^30.
 int check_operands(int transa, int transb, int M, int N, int K, const float* A, int lda,
                    const float* B, int ldb, const float* C, int ldc);
 

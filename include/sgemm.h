@@ -21,6 +21,8 @@
  * written; elements of A and B outside their logical extents are never read
  * (the tile loads substitute zeros there, ibid. §3 "boundary check 후 0-padding").
  * K == 0 writes zeros to C (the empty sum).  M == 0 or N == 0 is a no-op.
+ * M, N and K may each be at most 2^30 (the kernels keep tile bounds in 32-bit
+ * integers; element offsets are 64-bit); larger ones return SGEMM_ERR_UNSUPPORTED.
  *
  * Memory.  A, B and C are DEVICE pointers owned by the caller.  C must not
  * overlap A or B.  Any alignment of pointers and leading dimensions is accepted;
@@ -57,7 +59,8 @@ typedef enum {
     SGEMM_ERR_INVALID_ARG = -1,   /* bad size, leading dimension, null or aliased pointer */
     SGEMM_ERR_ALIGNMENT = -2,     /* reserved: misalignment selects another kernel instead */
     SGEMM_ERR_LAUNCH = -3,        /* a CUDA call failed (message: sgemm_last_error()) */
-    SGEMM_ERR_UNSUPPORTED = -4,   /* no device, wrong architecture, unknown kernel id */
+    SGEMM_ERR_UNSUPPORTED = -4,   /* no device, wrong architecture, unknown kernel id,
+                                     M, N or K above 2^30 */
     SGEMM_ERR_TIMEOUT = -5,       /* a bounded device-side wait gave up */
     SGEMM_ERR_WORKSPACE = -6      /* caller workspace too small, or allocation failed */
 } sgemm_status;

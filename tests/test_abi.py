@@ -90,6 +90,42 @@ def test_invalid_arguments_rejected_before_launch(lib, args):
     assert lib.sgemm_last_error() != b""
 
 
+BIG = 2**30 + 1   # one past the largest dimension the kernels index in 32 bits
+
+
+@pytest.mark.parametrize("M,N,K", [(BIG, 4, 4), (4, BIG, 4), (4, 4, BIG)])
+def test_dimensions_above_2_30_are_refused_before_launch(lib, M, N, K):
+    """A dimension above 2^30 is refused by every entry point (nothing is planned);
+    the fake pointers are far enough apart that no overlap check fires first."""
+    from dense_fp32_gemm_09_gb300._abi import SgemmConfig
+    lda, ldb, ldc = max(K, 1), max(N, 1), max(N, 1)
+    a, b, c = P, P + (1 << 44), P + (1 << 45)
+    assert lib.sgemm_run(M, N, K, a, lda, b, ldb, c, ldc, None) == -4
+    assert b"2^30" in lib.sgemm_last_error()
+    assert lib.sgemm_run_ws(M, N, K, a, lda, b, ldb, c, ldc, None, 0, None) == -4
+    assert lib.sgemm_run_ex(M, N, K, 1.0, a, lda, b, ldb, 0.0, c, ldc, -1, 0, None) == -4
+    assert lib.sgemm_run_noalloc(M, N, K, a, lda, b, ldb, c, ldc, None) == -4
+    assert lib.sgemm_tf32x3_run(M, N, K, a, lda, b, ldb, c, ldc, None) == -4
+    out = ctypes.c_size_t(0)
+    assert lib.sgemm_workspace_size(M, N, K, lda, ldb, ldc, None, None, None,
+                                    ctypes.byref(out)) == -4
+    assert lib.sgemm_tf32x3_workspace_size(M, N, K, ctypes.byref(out)) == -4
+    cfg = SgemmConfig()
+    assert lib.sgemm_query_config(M, N, K, lda, ldb, ldc, None, None, None,
+                                  ctypes.byref(cfg)) == -4
+    assert lib.sgemm_schedule_check(M, N, K, 0, 152, 1, 0, ctypes.byref(cfg)) == -4
+    n = ctypes.c_int(0)
+    assert lib.sgemm_host_plan_check(M, N, K, ctypes.byref(n), None, None) == -4
+
+
+def test_largest_dimension_is_planned(lib):
+    """2^30 itself is accepted: the host-side schedule walk plans it."""
+    from dense_fp32_gemm_09_gb300._abi import SgemmConfig
+    cfg = SgemmConfig()
+    assert lib.sgemm_schedule_check(2**30, 64, 64, 0, 152, 1, 0, ctypes.byref(cfg)) == 0
+    assert cfg.tiles > 0
+
+
 def test_empty_output_is_a_noop(lib):
     assert lib.sgemm_run(0, 5, 3, P, 3, P * 4, 5, P * 8, 5, None) == 0
     assert lib.sgemm_run(5, 0, 3, P, 3, P * 4, 1, P * 8, 1, None) == 0
