@@ -342,25 +342,37 @@ int plan(int M, int N, int K, const float* A, int lda, const float* B, int ldb, 
 // ----------------------------------------------------------------------------
 // Workspaces owned by the library: one per (device, stream), grown on demand
 // with the stream-ordered allocator so a resize never races in-flight work.
+// A call holds its workspace's lock from the lookup until its launches are
+// enqueued, so another host thread on the same stream cannot free the buffer
+// (by growing it) between this call's lookup and its launch; calls on other
+// streams take other locks.
 // ----------------------------------------------------------------------------
 struct Workspace {
+    std::mutex mu;
     void* ptr = nullptr;
     size_t bytes = 0;
 };
-std::mutex g_ws_mu;
+std::mutex g_ws_mu;   // guards the map itself; entries are stable until shutdown
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
 
-int library_workspace(cudaStream_t stream, size_t need, void** out) {
+int library_workspace(cudaStream_t stream, size_t need, void** out,
+                      std::unique_lock<std::mutex>* hold) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
         set_error("cudaGetDevice", e);
         return SGEMM_ERR_LAUNCH;
     }
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    Workspace& w = g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    Workspace* wp = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_ws_mu);
+        wp = &g_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    }
+    std::unique_lock<std::mutex> wl(wp->mu);
+    Workspace& w = *wp;
     if (w.bytes >= need) {
         *out = w.ptr;
+        *hold = std::move(wl);
         return SGEMM_OK;
     }
     if (w.ptr) {
@@ -381,6 +393,7 @@ int library_workspace(cudaStream_t stream, size_t need, void** out) {
     }
     w.bytes = bytes;
     *out = w.ptr;
+    *hold = std::move(wl);
     return SGEMM_OK;
 }
 
@@ -655,9 +668,11 @@ int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const fl
     p.args.beta = beta;
     p.args.status = status_word_ptr();
     p.args.epi = (beta != 0.0f) ? kEpiAlphaBeta : (alpha != 1.0f ? kEpiAlpha : kEpiPlain);
+    std::unique_lock<std::mutex> ws_hold;   // the library workspace, until launched
     if (pack) {
         void* base = nullptr;
-        rc = library_workspace(stream, bytes_a + bytes_b + p.ws_partial_bytes, &base);
+        rc = library_workspace(stream, bytes_a + bytes_b + p.ws_partial_bytes, &base,
+                               &ws_hold);
         if (rc != SGEMM_OK) return rc;
         char* w = static_cast<char*>(base);
         if (pack_a) {
@@ -682,7 +697,7 @@ int run_impl(int M, int N, int K, float alpha, const float* A, int lda, const fl
     if (need > 0) {
         void* base = nullptr;
         if (library_ws) {
-            rc = library_workspace(stream, need, &base);
+            rc = library_workspace(stream, need, &base, &ws_hold);
             if (rc != SGEMM_OK) return rc;
         } else {
             if (ws == nullptr || ws_bytes < need || !aligned16(ws)) {
@@ -986,8 +1001,9 @@ int sgemm_tf32x3_run_ex(int M, int N, int K, float alpha, const float* A, int ld
     if (rc != SGEMM_OK) return rc;
     if (K == 0 || alpha == 0.0f) return launch_scale(C, M, N, ldc, beta, s, d);
     const size_t need = tf32x3_workspace_bytes(M, N, K);
+    std::unique_lock<std::mutex> ws_hold;   // the library workspace, until launched
     if (ws == nullptr) {
-        rc = library_workspace(s, need, &ws);
+        rc = library_workspace(s, need, &ws, &ws_hold);
         if (rc != SGEMM_OK) return rc;
         ws_bytes = need;
     } else if (ws_bytes < need || !aligned16(ws)) {

@@ -32,6 +32,13 @@
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  * call is asynchronous on that stream and does not synchronise the host.
  *
+ * Threads.  Entry points may be called from several host threads at once.  Calls
+ * that use the library-owned workspace of one (device, stream) hold its lock from
+ * the workspace lookup until their launches are enqueued, so a call that grows
+ * it never frees a buffer another call is about to launch with; calls on other
+ * streams do not wait for each other.  sgemm_shutdown is the exception: it must
+ * not run concurrently with any other call.
+ *
  * Errors.  Every entry point returns an sgemm_status and never aborts the
  * process.  Invalid arguments are rejected before anything is launched.
  */
