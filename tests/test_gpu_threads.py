@@ -7,6 +7,7 @@ re-allocate it) while other threads are between their workspace lookup and
 their launch.  Every product must match the oracle and equal, bit for bit, the
 same call made alone (the kernels are deterministic); the second case gives each
 thread its own stream, so the products also run concurrently on the GPU."""
+import ctypes
 import threading
 
 import numpy as np
@@ -52,10 +53,20 @@ def test_threads_growing_one_workspace(cuda, oracle_mod, shared_stream):
     for i, (M, N, K, path) in enumerate(CALLS):
         A, B = random_pair(M, N, K, seed=60 + i)
         inputs.append((A, B, A.cuda(), B.cuda()))
-    # Workspace needs differ (and the 3xTF32 split operands need more than any
-    # partial tiles here), so the concurrent phase grows the workspace.
-    needs = {sgemm_workspace_size(M, N, K, K, N, N) for M, N, K, p in CALLS if p == "fp32"}
-    assert len(needs - {0}) >= 2
+    # Workspace needs: partial tiles take one sized by the grid (the same for every
+    # stream-K plan here), 3xTF32 its split operands, the staged ragged problem its
+    # aligned copies as well.  Every thread starts with the call that needs least,
+    # so the fresh stream's workspace is grown by the calls that follow.
+    needs = []
+    for M, N, K, p in CALLS:
+        if p == "fp32":
+            needs.append(sgemm_workspace_size(M, N, K, K, N, N))
+        else:
+            out = ctypes.c_size_t(0)
+            check(lib.sgemm_tf32x3_workspace_size(M, N, K, ctypes.byref(out)), "ws")
+            needs.append(out.value)
+    first = int(np.argmin([n if n > 0 else 1 << 62 for n in needs]))
+    assert len(set(needs) - {0}) >= 3 and needs[first] < max(needs)
     assert sgemm_query_config(1024, 1024, 1024)["sk_tiles"] > 0
 
     # Each call alone, on a stream of its own, checked against the oracle.
@@ -84,7 +95,8 @@ def test_threads_growing_one_workspace(cuda, oracle_mod, shared_stream):
     def worker(t):
         try:
             stream = streams[0 if shared_stream else t].cuda_stream
-            order = np.random.default_rng(t).permutation(len(CALLS))
+            rest = [j for j in range(len(CALLS)) if j != first]
+            order = [first] + [rest[i] for i in np.random.default_rng(t).permutation(len(rest))]
             barrier.wait()
             for r in range(ROUNDS):
                 for j in order:
