@@ -64,7 +64,9 @@ int find_entry(const char* name) {
     return -1;
 }
 
-// Per-device facts and per-(device, entry) residency, computed once.
+// Per-device facts and per-(device, entry) residency, computed once per device
+// (and again after sgemm_shutdown), with each kernel's shared-memory attributes
+// set in the device's context on the way.
 struct DeviceInfo {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
@@ -1169,6 +1171,13 @@ int sgemm_shutdown(void) {
     g_ws.clear();
     shutdown_host_pipes();
     forget_noalloc_scratch();
+    forget_tf32x3_attributes();
+    {
+        // Kernel attributes live in the device's context: a context made after a
+        // device reset needs them set again, so the per-device facts are redone.
+        std::lock_guard<std::mutex> ld(g_dev_mu);
+        g_dev.clear();
+    }
     return rc;
 }
 

@@ -39,6 +39,10 @@ int check_operands(int transa, int transb, int M, int N, int K, const float* A, 
 // Destroys the host-buffer entry point's streams and events (sgemm_shutdown).
 void shutdown_host_pipes();
 
+// Forgets which devices had the 3xTF32 kernels' shared-memory limit raised
+// (sgemm_shutdown): the next launch on each device sets it again.
+void forget_tf32x3_attributes();
+
 // Drops the cached device addresses of sgemm_run_noalloc's static scratch
 // (sgemm_shutdown); the next call looks them up again.
 void forget_noalloc_scratch();

@@ -702,6 +702,12 @@ int tf32x3_prepare(int M, int N, int K, const float* A, long long lda, const flo
 
 namespace {
 
+// The shared-memory limit is an attribute of the kernel in each device's context:
+// it is raised once per (tile width, device) and forgotten by sgemm_shutdown, so a
+// context created after a device reset gets it again.
+std::mutex g_attr_mu;
+std::vector<int> g_attr_done[2];   // [BN == 256][device]: 0 not yet, 1 done
+
 template <int BN>
 int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long long ldc,
                    int c_vec, const WsLayout& L, const float* a_hi, long long lda_hi,
@@ -709,17 +715,14 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
                    int* launches) {
     using namespace tc;
     using V = Variant<BN>;
-    // The shared-memory limit is an attribute of the kernel in each device's
-    // context: raise it once per device this process launches on.
-    static std::mutex attr_mu;
-    static std::vector<int> attr_done;   // per device: 0 not yet, 1 done
     {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) {
             set_last_error_message("tf32x3: cudaGetDevice failed");
             return SGEMM_ERR_LAUNCH;
         }
-        std::lock_guard<std::mutex> lk(attr_mu);
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        std::vector<int>& attr_done = g_attr_done[BN == 256 ? 1 : 0];
         if (static_cast<int>(attr_done.size()) <= dev) attr_done.resize(dev + 1, 0);
         if (!attr_done[dev]) {
             if (cudaFuncSetAttribute(tf32x3_kernel<BN, V::kBK, V::kStages>,
@@ -775,6 +778,11 @@ int launch_variant(int M, int N, int K, float alpha, float beta, float* C, long 
 }
 
 }  // namespace
+
+void forget_tf32x3_attributes() {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    for (auto& v : g_attr_done) v.clear();
+}
 
 int tf32x3_tile_width(int M, int N, int K, int sms) {
     return tf32x3_choice(M, N, K, sms).bn;

@@ -362,8 +362,12 @@ SGEMM_API const char* sgemm_last_error(void);
 /* Kernels this library has launched in this process (for launch accounting). */
 SGEMM_API uint64_t sgemm_launch_count(void);
 
-/* Frees the library-owned workspaces on every device.  Not thread-safe with
- * concurrent sgemm_run calls; call it when the library is no longer in use. */
+/* Frees the library-owned workspaces on every device, destroys the host-buffer
+ * entry point's streams and events, and forgets the per-device state the library
+ * keeps (kernel attributes set in the device's context, the allocation-free
+ * entry's scratch addresses).  The library can be used again afterwards,
+ * including after cudaDeviceReset: that state is set up again on first use.  Not
+ * thread-safe with any concurrent call into the library. */
 SGEMM_API int sgemm_shutdown(void);
 
 #ifdef __cplusplus
