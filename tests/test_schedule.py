@@ -30,6 +30,10 @@ def test_schedule_covers_each_slice_once(lib, schedule):
         assert cfg.tiles == -(-M // cfg.bm) * -(-N // cfg.bn)
         if schedule == 1:
             assert cfg.sk_tiles == 0 and cfg.split_k == 1
+        if cfg.sk_tiles > 0 and cfg.cluster == 0:
+            # Stream-K shares its split tiles among more CTAs than there are such
+            # tiles, so the reduction launch always has partial tiles to sum.
+            assert cfg.sk_tiles < cfg.grid and cfg.split_k >= 2, (kid, M, N, K, sms, occ)
 
 
 def test_stream_k_balances_a_partial_last_wave(lib):
