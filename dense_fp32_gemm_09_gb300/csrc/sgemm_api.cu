@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <cstdint>
 #include <cstdio>
@@ -71,6 +72,10 @@ struct DeviceInfo {
     int sms = 0;
     int cc_major = 0, cc_minor = 0;
     std::vector<int> occ;  // resident CTAs per SM for each table entry (0 = unusable)
+    // Clusters of 2, 4 and 8 CTAs of each entry that can be resident at once
+    // (cudaOccupancyMaxActiveClusters).  A cluster must sit inside one GPC, so at
+    // one CTA per SM only 15 clusters of 8 fit on 152 SMs, not 19.
+    std::vector<std::array<int, 3>> clusters;
 };
 
 std::mutex g_dev_mu;
@@ -101,6 +106,7 @@ int device_info(int dev, const DeviceInfo** out) {
     }
     const auto& t = table();
     info.occ.assign(t.size(), 0);
+    info.clusters.assign(t.size(), {0, 0, 0});
     for (size_t i = 0; i < t.size(); ++i) {
         e = cudaFuncSetAttribute(t[i].kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  t[i].smem_bytes);
@@ -116,6 +122,28 @@ int device_info(int dev, const DeviceInfo** out) {
             return SGEMM_ERR_LAUNCH;
         }
         info.occ[i] = occ;
+        info.clusters[i] = {0, 0, 0};
+        if (t[i].tma || occ <= 0) continue;   // only the cp.async kernels sum in clusters
+        for (int l = 0; l < 3; ++l) {
+            const unsigned S = 2u << l;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = S;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cudaLaunchConfig_t c{};
+            c.gridDim = dim3(S);
+            c.blockDim = dim3(static_cast<unsigned>(t[i].threads));
+            c.dynamicSmemBytes = static_cast<size_t>(t[i].smem_bytes);
+            c.attrs = at;
+            c.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, t[i].kernel, &c) != cudaSuccess) {
+                cudaGetLastError();   // a size the kernel cannot take: never chosen
+                n = 0;
+            }
+            info.clusters[i][l] = n;
+        }
     }
     auto res = g_dev.emplace(dev, std::move(info));
     *out = &res.first->second;
@@ -234,26 +262,44 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
     else if (v4 && N <= 128 && M >= 4096)
         // A 256-wide tile would compute half its columns for nothing.
         name = "256x128x64_t8x16_s2_f2_v4";
-    else if (tiles128 * 4 < sms)
-        name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
-    else if (v4) {
+    else if (tiles128 * 4 < sms) {
+        // Small C.  With K >= 2048 every tile's long K range is shared out (stream-K
+        // or a cluster split), and larger register tiles beat 64 x 64 ones where
+        // their tiles cover C with at most a fifth of their area to spare: 128 x 256
+        // from 4 such tiles (768 x 768 x 4096: 49.9 against 41.9 TFLOP/s; 512 x 512
+        // x 8192: 50.8 against 37.2; 256 x 512 x 8192: 43.1 against 37.7), else 128
+        // x 128 from 9 (384 x 384 x 2048: 26.1 against 22.1).  320 x 320 x 4096,
+        // whose 128-wide tiles would be a third empty, stays on 64 x 64 tiles
+        // (25.1 against 22.4).
+        const long long tiles_w = static_cast<long long>((M + 127) / 128) * ((N + 255) / 256);
+        const double area = static_cast<double>(M) * N;
+        const bool wide_ok = tiles_w >= 4 && area >= 0.8 * tiles_w * (128.0 * 256.0);
+        const bool quad_ok = tiles128 >= 9 && area >= 0.8 * tiles128 * (128.0 * 128.0);
+        if (v4 && K >= 2048 && (wide_ok || quad_ok))
+            name = wide_ok ? "128x256x32_t8x16_s4_f2_v4" : "128x128x32_t8x8_s3_f2_v4";
+        else
+            name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
+    } else if (v4) {
         // 64-deep slices run about 3% faster; 32-deep ones share K out more finely
         // over the stream-K ranges.  The deeper ones win once every CTA gets about
         // 20 of them (measured from 1536^3, where they lose, to 4096x4096x1536).
         // Among the 64-deep entries the one with double-buffered fragments (128 x
-        // 256) wins once K >= 2048 and its tiles fill at least two waves (4096^3
-        // 65.4 against 64.1 TFLOP/s, 8192^3 66.5 against 64.9); with less than
-        // that the 256 x 128 entry does (2048^3 59.4 against 58.5, 3008 x 2048 x
-        // 2000 55.6 against 54.6).  Of the 32-deep ones the 128 x 256 tile is the
-        // faster (1536^3 53.4 against 52.6, 1024^3 equal).
+        // 256) wins once every CTA gets about 44 of its slices (4096^3 65.9 against
+        // 64.4 TFLOP/s, 8192^3 67.1 against 65.2, 3072^3 64.1 against 63.2,
+        // 4096 x 4096 x 1024 62.5 against 61.8, 8192 x 8192 x 512 63.0 against
+        // 62.0); with fewer the 256 x 128 entry does (2048^3 59.4 against 58.9,
+        // 2560 x 2560 x 1280 58.4 against 57.2, 3008 x 2048 x 2000 55.6 against
+        // 54.6).  Of the 32-deep ones the 128 x 256 tile is the faster (1536^3 53.4
+        // against 52.6, 1024^3 equal).
         const long long slices64 =
             static_cast<long long>((M + 255) / 256) * ((N + 127) / 128) * ((K + 63) / 64);
         const long long tiles_w = static_cast<long long>((M + 127) / 128) * ((N + 255) / 256);
+        const long long per_cta64 = tiles_w * ((K + 63) / 64) / sms;
         // The 256 x 128 entry spreads its refills except on tiles crossing M or N;
         // with such tiles and under 1.5 waves its all-burst twin is faster.
         const long long tiles_h = static_cast<long long>((M + 255) / 256) * ((N + 127) / 128);
         const bool ragged_h = (M % 256 != 0 || N % 128 != 0) && 2 * tiles_h < 3LL * sms;
-        if (K >= 2048 && tiles_w >= 2LL * sms)
+        if (per_cta64 >= 44 && !ragged_h)
             name = "128x256x64_t8x16_s2_f2_v4";
         else if (K >= 2048 || slices64 >= 20LL * sms)
             name = ragged_h ? "256x128x64_t8x16_s2_f2_v4_burst" : "256x128x64_t8x16_s2_f2_v4";
@@ -286,7 +332,15 @@ double store_cost_slices(const KernelEntry& e) { return 12.0 / e.bk; }
 // SGEMM_SK_GAP=<n> asks for that stream-K gap where it is allowed;
 // SGEMM_GROUP_M=<n> sets the raster group height; SGEMM_CLUSTER=<S> asks for
 // clusters of up to S CTAs per tile where allowed, 0 for none (tuning).
-void make_schedule(int sms, int occ, int entry, int schedule, Plan& p) {
+// `clusters` (null on the host-only checks): the entry's co-resident clusters of
+// 2, 4 and 8 CTAs.  Where the automatic split means one wave of T clusters (T*S
+// CTAs within the resident slots), it takes only a cluster size whose T clusters
+// can all be resident at once: a second wave of clusters doubles the time
+// (768 x 768 x 8192 on 128 x 256 x 32 tiles: 18 clusters of 8 where 15 fit ran
+// below 38.3 TFLOP/s; stream-K over all 152 SMs instead, 56.0).  Splits that fill the SMs several times over
+// by design are left alone.
+void make_schedule(int sms, int occ, int entry, int schedule, Plan& p,
+                   const std::array<int, 3>* clusters = nullptr) {
     const KernelEntry& e = table()[entry];
     int forced_gap = -1, group_m = 0, forced_cluster = -1;
     if (const char* g = std::getenv("SGEMM_SK_GAP")) forced_gap = std::atoi(g);
@@ -294,7 +348,18 @@ void make_schedule(int sms, int occ, int entry, int schedule, Plan& p) {
     if (const char* g = std::getenv("SGEMM_CLUSTER")) forced_cluster = std::max(0, std::atoi(g));
     // The cp.async kernels sum cluster-split tiles in distributed shared memory;
     // the TMA-fed ones only take the stream-K reduction.
-    const int cluster_max = e.tma ? 0 : kMaxCluster;
+    int cluster_max = e.tma ? 0 : kMaxCluster;
+    if (clusters != nullptr && schedule == 0 && forced_cluster < 0) {
+        const long long T = static_cast<long long>((p.args.M + e.bm - 1) / e.bm) *
+                            ((p.args.N + e.bn - 1) / e.bn);
+        int l = 2;   // cluster_max = 2 << l
+        while (cluster_max >= 2 && T * cluster_max <= static_cast<long long>(sms) * occ &&
+               (*clusters)[l] < T) {
+            cluster_max /= 2;
+            --l;
+        }
+        if (cluster_max < 2) cluster_max = 0;
+    }
     const SchedSizes z = plan_schedule(p.args, e.bm, e.bn, e.bk, sms, occ, schedule,
                                        store_cost_slices(e), forced_gap < 0 ? -1 : forced_gap,
                                        group_m, cluster_max, forced_cluster);
@@ -337,7 +402,7 @@ int plan(int M, int N, int K, const float* A, int lda, const float* B, int ldb, 
     a.A = A; a.B = B; a.C = C;
     a.lda = lda; a.ldb = ldb; a.ldc = ldc;
     a.c_vec = (aligned16(C) && ldc % 4 == 0) ? 1 : 0;
-    make_schedule(d->sms, d->occ[entry], entry, schedule, p);
+    make_schedule(d->sms, d->occ[entry], entry, schedule, p, &d->clusters[entry]);
     return SGEMM_OK;
 }
 

@@ -166,7 +166,7 @@ __host__ __device__ __forceinline__ void tile_origin(const GemmArgs& a, int tile
 // ----------------------------------------------------------------------------
 // Host-side planning of the schedule above
 // ----------------------------------------------------------------------------
-constexpr int kMinSkIters = 4;   // fewest k-slices a CTA gets when tiles are split
+constexpr int kMinSkIters = 4;   // fewest k-slices a CTA gets when all tiles are split
 constexpr size_t kWsAlign = 256;
 constexpr int kMaxSkTiles = 16384;   // ceiling on the persistent grid
 constexpr int kMaxSplit = 256;       // most CTAs that may share one split tile
@@ -352,12 +352,17 @@ inline SchedSizes plan_schedule(GemmArgs& a, int bm, int bn, int bk, int sms, in
     long long G, dp, sk;
     if (T >= Gmax) {
         // Whole waves run data-parallel; a partial last wave is shared out by
-        // k-slices when every CTA gets enough of them.
+        // k-slices when every CTA gets at least one and the shared tail (its
+        // slices plus about two slices of partial stores and reduction) is
+        // shorter than the extra wave of whole tiles it replaces: 4096 x 4096 x
+        // 512 on 128 x 256 x 64 tiles, 56 tiles of 8 slices past 3 waves, ran
+        // 52.7 TFLOP/s with the extra wave, where its 32-deep twin, whose 16
+        // slices a tile let stream-K take those tiles, ran 57.3.
         G = Gmax;
         const long long rem = T % Gmax;
-        const bool use_sk = rem != 0 && schedule != 1 &&
-                            (schedule == 2 ? rem * a.KT >= Gmax
-                                           : rem * a.KT >= Gmax * kMinSkIters);
+        const long long tail = (rem * a.KT + Gmax - 1) / Gmax;   // slices per CTA
+        const bool use_sk = rem != 0 && schedule != 1 && rem * a.KT >= Gmax &&
+                            (schedule == 2 || tail + 2 < a.KT);
         sk = use_sk ? rem : 0;
         dp = T - sk;
     } else {

@@ -450,13 +450,16 @@ def test_query_config_matches_bench_choice(cuda):
     (512, 512, 512, "64x64x16_t8x8_s3_f2_v4"),
     (2048, 4096, 1024, "256x128x64_t8x16_s2_f2_v4"),
     (3008, 2048, 2000, "256x128x64_t8x16_s2_f2_v4_burst"),
+    (4096, 4096, 1024, "128x256x64_t8x16_s2_f2_v4"),
+    (768, 768, 4096, "128x256x32_t8x16_s4_f2_v4"),
+    (384, 384, 4096, "128x128x32_t8x8_s3_f2_v4"),
 ])
 def test_narrow_c_tile_choice(cuda, M, N, K, name):
     """Narrow C gets tiles no wider than it: 512 x 64 for N <= 64 once M fills eight
     of them, 256 x 128 for N <= 128.  Square-ish C takes 64-deep slices when K >= 2048
     or every CTA gets about 20 of them (128 x 256 tiles with double-buffered fragments
-    once K >= 2048 and they fill two waves), 32-deep ones on 128 x 256 tiles below;
-    the smallest problems take 32 x 32 tiles."""
+    once every CTA gets about 44), 32-deep ones on 128 x 256 tiles below; the
+    smallest problems take 32 x 32 tiles."""
     assert sgemm_query_config(M, N, K)["name"] == name
 
 

@@ -50,6 +50,32 @@ def test_stream_k_balances_a_partial_last_wave(lib):
     assert cfg.sk_tiles == 0 and cfg.grid == 152
 
 
+def test_partial_last_wave_goes_to_stream_k_when_that_shortens_it(lib):
+    """Past whole waves, the leftover tiles are shared by k-slices when every CTA gets
+    one and the shared tail, plus about two slices of stores and reduction, is
+    shorter than another wave of whole tiles."""
+    kid = _kid(lib, "128x256x64_t8x16_s2_f2_v4")
+    # 4096 x 4096 x 512: 512 tiles = 3 waves + 56 tiles of 8 slices; 448 slices give
+    # every CTA 3, and 3 + 2 < 8.
+    cfg = _cfg()
+    assert lib.sgemm_schedule_check(4096, 4096, 512, kid, 152, 1, 0, ctypes.byref(cfg)) == 0
+    assert (cfg.tiles, cfg.grid, cfg.sk_tiles) == (512, 152, 56) and cfg.split_k >= 2
+    # 4 slices a tile: 224 slices give 2 a CTA, and 2 + 2 is not shorter than 4.
+    cfg = _cfg()
+    assert lib.sgemm_schedule_check(4096, 4096, 256, kid, 152, 1, 0, ctypes.byref(cfg)) == 0
+    assert (cfg.tiles, cfg.grid, cfg.sk_tiles) == (512, 152, 0)
+    # 153 tiles of 64 slices: the one leftover tile has fewer slices than CTAs.
+    cfg = _cfg()
+    assert lib.sgemm_schedule_check(9 * 128, 17 * 256, 4096, kid, 152, 1, 0,
+                                    ctypes.byref(cfg)) == 0
+    assert (cfg.tiles, cfg.grid, cfg.sk_tiles) == (153, 152, 0)
+    # 155 tiles of 64 slices: 192 leftover slices, 2 a CTA: shared.
+    cfg = _cfg()
+    assert lib.sgemm_schedule_check(5 * 128, 31 * 256, 4096, kid, 152, 1, 0,
+                                    ctypes.byref(cfg)) == 0
+    assert (cfg.tiles, cfg.grid, cfg.sk_tiles) == (155, 152, 3)
+
+
 def test_small_problem_splits_k(lib, monkeypatch):
     monkeypatch.setenv("SGEMM_CLUSTER", "0")   # the stream-K form of the split
     table = [lib.sgemm_kernel_name(i).decode() for i in range(lib.sgemm_num_kernels())]

@@ -20,17 +20,22 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
 
 
 @pytest.mark.parametrize("shape,expected", [
-    # Square and large: 64-deep slices once K >= 2048; double-buffered fragments on
-    # 128 x 256 tiles when those fill two waves (4096^3: 32*16 = 512 >= 2*152) ...
+    # 64-deep slices on 128 x 256 tiles with double-buffered fragments once every
+    # CTA gets at least 44 of them (tiles of 128 x 256 times 64-deep slices a tile,
+    # over 152 SMs) ...
     ((4096, 4096, 4096), "128x256x64_t8x16_s2_f2_v4"),
     ((8192, 8192, 8192), "128x256x64_t8x16_s2_f2_v4"),
-    ((4864, 4864, 2048), "128x256x64_t8x16_s2_f2_v4"),  # 38*19 = 722 tiles
-    ((2048, 4864, 2048), "128x256x64_t8x16_s2_f2_v4"),  # 16*19 = 304: two waves exactly
-    ((1920, 4864, 2048), "256x128x64_t8x16_s2_f2_v4"),  # 15*19 = 285 < 304
-    ((2048, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),  # 16*8 = 128 < 304
-    ((4096, 4096, 2044), "256x128x64_t8x16_s2_f2_v4"),  # K below 2048
-    # ... or once every CTA gets about 20 of them (16*32*24 = 12288 >= 20*152) ...
-    ((4096, 4096, 1536), "256x128x64_t8x16_s2_f2_v4"),
+    ((4864, 4864, 2048), "128x256x64_t8x16_s2_f2_v4"),  # 722 tiles * 32 / 152 = 152
+    ((1920, 4864, 2048), "128x256x64_t8x16_s2_f2_v4"),  # 285 * 32 / 152 = 60
+    ((4096, 4096, 2044), "128x256x64_t8x16_s2_f2_v4"),  # 512 * 32 / 152 = 107
+    ((4096, 4096, 1536), "128x256x64_t8x16_s2_f2_v4"),  # 512 * 24 / 152 = 80
+    ((8192, 8192, 512), "128x256x64_t8x16_s2_f2_v4"),   # 2048 * 8 / 152 = 107
+    ((3072, 3072, 1536), "128x256x64_t8x16_s2_f2_v4"),  # 288 * 24 / 152 = 45
+    # ... else 64-deep slices on 256 x 128 tiles once K >= 2048 or every CTA gets
+    # about 20 of them ...
+    ((2048, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),  # 128 * 32 / 152 = 26
+    ((2560, 2560, 1280), "256x128x64_t8x16_s2_f2_v4"),  # 200 * 20 / 152 = 26
+    ((4096, 4096, 768), "256x128x64_t8x16_s2_f2_v4"),   # 512 * 12 / 152 = 40
     # ... else 32-deep slices on 128 x 256 tiles (1024^3: 4*8*16 = 512 64-deep
     # slices; 1536^3: 1728).
     ((1024, 1024, 1024), "128x256x32_t8x16_s4_f2_v4"),
@@ -40,8 +45,9 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     # Tiles crossing M or N with under 1.5 waves of 256 x 128 tiles: the all-burst twin.
     ((3008, 2048, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # 12*16 = 192 < 228
     ((3500, 2048, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # 14*16 = 224
-    ((3584, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),        # no tile crosses M or N
-    ((3600, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),        # 15*16 = 240 tiles
+    ((3584, 2048, 2048), "128x256x64_t8x16_s2_f2_v4"),        # no tile crosses: 47 a CTA
+    ((3600, 2048, 2048), "128x256x64_t8x16_s2_f2_v4"),        # 15*16 = 240 tiles: 48 a CTA
+    ((2816, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),        # 11*16 tiles, 41 a CTA
     ((2048, 2000, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # N edge, 8*16 tiles
     # The smallest problems: at most SMs/4 tiles of 64 x 64 and K <= 1024.
     ((256, 256, 256), "32x32x16_t4x4_s3_f2_v4"),
@@ -49,7 +55,16 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     ((384, 384, 1024), "32x32x16_t4x4_s3_f2_v4"),
     ((384, 384, 1028), "64x64x16_t8x8_s3_f2_v4"),    # K too deep: few 128 tiles -> 64 x 64
     ((448, 384, 384), "64x64x16_t8x8_s3_f2_v4"),     # 42 tiles of 64^2: 168 > 152
-    ((256, 256, 2048), "64x64x16_t8x8_s3_f2_v4"),
+    ((256, 256, 2048), "64x64x16_t8x8_s3_f2_v4"),    # 4 tiles of 128^2: 64 x 64 stays
+    # Small C (fewer than SMs/4 tiles of 128^2) with K >= 2048: 128 x 256 tiles from 4
+    # of them covering C with at most a fifth to spare, else 128 x 128 from 9.
+    ((384, 384, 2048), "128x128x32_t8x8_s3_f2_v4"),   # 6 wide tiles, 25 % spare: 128^2
+    ((512, 512, 2048), "128x256x32_t8x16_s4_f2_v4"),  # 8 wide tiles, none spare
+    ((256, 512, 8192), "128x256x32_t8x16_s4_f2_v4"),  # 4 wide tiles
+    ((640, 640, 4096), "128x256x32_t8x16_s4_f2_v4"),  # 15 wide tiles, 17 % spare
+    ((768, 768, 8192), "128x256x32_t8x16_s4_f2_v4"),
+    ((320, 320, 4096), "64x64x16_t8x8_s3_f2_v4"),     # both larger tiles a third empty
+    ((768, 768, 2044), "64x64x16_t8x8_s3_f2_v4"),     # K below 2048
     # Narrow C (N <= 64): 512-row tiles once M >= 4096, else 64 x 64.
     ((16384, 64, 4096), "512x64x32_t8x16_s2_f2_v4"),
     ((4096, 36, 100), "512x64x32_t8x16_s2_f2_v4"),
