@@ -265,15 +265,18 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
     else if (tiles128 * 4 < sms) {
         // Small C.  With K >= 2048 every tile's long K range is shared out (stream-K
         // or a cluster split), and larger register tiles beat 64 x 64 ones where
-        // their tiles cover C with at most a fifth of their area to spare: 128 x 256
-        // from 4 such tiles (768 x 768 x 4096: 49.9 against 41.9 TFLOP/s; 512 x 512
-        // x 8192: 50.8 against 37.2; 256 x 512 x 8192: 43.1 against 37.7), else 128
-        // x 128 from 9 (384 x 384 x 2048: 26.1 against 22.1).  320 x 320 x 4096,
-        // whose 128-wide tiles would be a third empty, stays on 64 x 64 tiles
-        // (25.1 against 22.4).
+        // they cover C closely: 128 x 256 tiles from 8 of them with at most a
+        // quarter of their area to spare, or from 4 with at most a tenth (768 x 768
+        // x 4096: 49.9 against 41.9 TFLOP/s; 512 x 512 x 8192: 50.8 against 37.2;
+        // 448 x 448 x 4096: 31.7 against 27.4; 256 x 512 x 8192: 43.1 against
+        // 37.7), else 128 x 128 tiles from 9 with at most a fifth to spare (384 x
+        // 384 x 2048: 26.0 against 22.1, where the six 128 x 256 tiles, a quarter
+        // empty, fall behind both).  320 x 320 x 4096, whose larger tiles would be a
+        // third empty, stays on 64 x 64 tiles (25.1 against 22.4).
         const long long tiles_w = static_cast<long long>((M + 127) / 128) * ((N + 255) / 256);
         const double area = static_cast<double>(M) * N;
-        const bool wide_ok = tiles_w >= 4 && area >= 0.8 * tiles_w * (128.0 * 256.0);
+        const bool wide_ok = tiles_w >= 4 && area >= (tiles_w >= 8 ? 0.75 : 0.9) * tiles_w *
+                                                         (128.0 * 256.0);
         const bool quad_ok = tiles128 >= 9 && area >= 0.8 * tiles128 * (128.0 * 128.0);
         if (v4 && K >= 2048 && (wide_ok || quad_ok))
             name = wide_ok ? "128x256x32_t8x16_s4_f2_v4" : "128x128x32_t8x8_s3_f2_v4";

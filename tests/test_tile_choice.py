@@ -56,9 +56,11 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     ((384, 384, 1028), "64x64x16_t8x8_s3_f2_v4"),    # K too deep: few 128 tiles -> 64 x 64
     ((448, 384, 384), "64x64x16_t8x8_s3_f2_v4"),     # 42 tiles of 64^2: 168 > 152
     ((256, 256, 2048), "64x64x16_t8x8_s3_f2_v4"),    # 4 tiles of 128^2: 64 x 64 stays
-    # Small C (fewer than SMs/4 tiles of 128^2) with K >= 2048: 128 x 256 tiles from 4
-    # of them covering C with at most a fifth to spare, else 128 x 128 from 9.
+    # Small C (fewer than SMs/4 tiles of 128^2) with K >= 2048: 128 x 256 tiles from 8
+    # of them with at most a quarter to spare or from 4 with at most a tenth, else
+    # 128 x 128 from 9 with at most a fifth.
     ((384, 384, 2048), "128x128x32_t8x8_s3_f2_v4"),   # 6 wide tiles, 25 % spare: 128^2
+    ((448, 448, 4096), "128x256x32_t8x16_s4_f2_v4"),  # 8 wide tiles, 23 % spare
     ((512, 512, 2048), "128x256x32_t8x16_s4_f2_v4"),  # 8 wide tiles, none spare
     ((256, 512, 8192), "128x256x32_t8x16_s4_f2_v4"),  # 4 wide tiles
     ((640, 640, 4096), "128x256x32_t8x16_s4_f2_v4"),  # 15 wide tiles, 17 % spare
