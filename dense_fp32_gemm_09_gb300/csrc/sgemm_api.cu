@@ -250,8 +250,10 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
     const long long tiles128 = static_cast<long long>((M + 127) / 128) * ((N + 127) / 128);
     const long long tiles64 = static_cast<long long>((M + 63) / 64) * ((N + 63) / 64);
     const char* name;
-    if (v4 && N <= 64 && M >= 4096)
-        // Narrow C: 512-row tiles once M fills 8 of them.
+    if (v4 && N <= 64 && M >= 2560)
+        // Narrow C: 512-row tiles once M fills 5 of them (3000 x 64 x 3000: 25.2
+        // TFLOP/s against 22.2 on 64 x 64 tiles; at 2048 x 64 x 4096 the 64 x 64
+        // tiles were ahead, 27.8 against 27.1).
         name = "512x64x32_t8x16_s2_f2_v4";
     else if (v4 && tiles64 * 4 <= sms && K <= 1024)
         // The smallest problems: 32 x 32 tiles give the SMs four times as many
@@ -259,9 +261,28 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
         name = "32x32x16_t4x4_s3_f2_v4";
     else if (v4 && N <= 64)
         name = "64x64x16_t8x8_s3_f2_v4";
-    else if (v4 && N <= 128 && M >= 4096)
-        // A 256-wide tile would compute half its columns for nothing.
-        name = "256x128x64_t8x16_s2_f2_v4";
+    else if (v4 && M <= 64)
+        // Short, wide C: tiles no taller than C (64 x 8192 x 4096: 37.2 TFLOP/s on
+        // 64 x 64 tiles against 14.5 on 256 x 128; 32 x 16384 x 4096: 24.6 on 32 x 32
+        // against 7.5).
+        name = M <= 32 ? "32x32x16_t4x4_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v4";
+    else if (v4 && M >= 4096 && N <= 256 && (N + 63) / 64 * 64 < (N + 127) / 128 * 128)
+        // Narrow C whose width 64-wide tiles fit more closely than 128-wide ones
+        // (8192 x 192 x 4096: 55.5 on 512 x 64 tiles against 43.3 on 256 x 128).
+        name = "512x64x32_t8x16_s2_f2_v4";
+    else if (v4 && N <= 128 && M >= 4096) {
+        // A 256-wide tile would compute half its columns for nothing.  How deep the
+        // slices of the 256 x 128 tiles can be depends on how many there are to
+        // share out: 64-deep from 4 a CTA (8192 x 128 x 8192, 4096 x 96 x 4096),
+        // 32-deep from 1.25 (4096 x 128 x 1024: 32.1 TFLOP/s against 20.7 for
+        // 64-deep; 8192 x 128 x 1024: 41.4 against 39.9), else 128 x 128 tiles
+        // (4096 x 128 x 512: 23.2 against 16.1).
+        const long long slices_h =
+            static_cast<long long>((M + 255) / 256) * ((N + 127) / 128) * ((K + 63) / 64);
+        name = slices_h >= 4LL * sms ? "256x128x64_t8x16_s2_f2_v4"
+             : 4 * slices_h >= 5LL * sms ? "256x128x32_t8x16_s4_f2_v4"
+                                         : "128x128x32_t8x8_s3_f2_v4";
+    }
     else if (tiles128 * 4 < sms) {
         // Small C.  With K >= 2048 every tile's long K range is shared out (stream-K
         // or a cluster split), and larger register tiles beat 64 x 64 ones where
@@ -273,13 +294,19 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
         // 384 x 2048: 26.0 against 22.1, where the six 128 x 256 tiles, a quarter
         // empty, fall behind both).  320 x 320 x 4096, whose larger tiles would be a
         // third empty, stays on 64 x 64 tiles (25.1 against 22.4).
-        const long long tiles_w = static_cast<long long>((M + 127) / 128) * ((N + 255) / 256);
+        // With N <= 128 the 256 x 128 orientation of the same tile fits C's width
+        // (2048 x 128 x 2048: 32.1 against 30.3 on 128 x 128 tiles).
+        const bool tall = N <= 128;
+        const long long tiles_w = tall
+            ? static_cast<long long>((M + 255) / 256) * ((N + 127) / 128)
+            : static_cast<long long>((M + 127) / 128) * ((N + 255) / 256);
         const double area = static_cast<double>(M) * N;
         const bool wide_ok = tiles_w >= 4 && area >= (tiles_w >= 8 ? 0.75 : 0.9) * tiles_w *
                                                          (128.0 * 256.0);
         const bool quad_ok = tiles128 >= 9 && area >= 0.8 * tiles128 * (128.0 * 128.0);
         if (v4 && K >= 2048 && (wide_ok || quad_ok))
-            name = wide_ok ? "128x256x32_t8x16_s4_f2_v4" : "128x128x32_t8x8_s3_f2_v4";
+            name = wide_ok ? (tall ? "256x128x32_t8x16_s4_f2_v4" : "128x256x32_t8x16_s4_f2_v4")
+                           : "128x128x32_t8x8_s3_f2_v4";
         else
             name = v4 ? "64x64x16_t8x8_s3_f2_v4" : "64x64x16_t8x8_s3_f2_v1";
     } else if (v4) {

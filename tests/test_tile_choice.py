@@ -67,14 +67,35 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     ((768, 768, 8192), "128x256x32_t8x16_s4_f2_v4"),
     ((320, 320, 4096), "64x64x16_t8x8_s3_f2_v4"),     # both larger tiles a third empty
     ((768, 768, 2044), "64x64x16_t8x8_s3_f2_v4"),     # K below 2048
-    # Narrow C (N <= 64): 512-row tiles once M >= 4096, else 64 x 64.
+    # Narrow C (N <= 64): 512-row tiles once M >= 2560, else 64 x 64.
     ((16384, 64, 4096), "512x64x32_t8x16_s2_f2_v4"),
     ((4096, 36, 100), "512x64x32_t8x16_s2_f2_v4"),
-    ((4095, 64, 4096), "64x64x16_t8x8_s3_f2_v4"),
+    ((3000, 64, 3000), "512x64x32_t8x16_s2_f2_v4"),
+    ((2560, 64, 4096), "512x64x32_t8x16_s2_f2_v4"),
+    ((2559, 64, 4096), "64x64x16_t8x8_s3_f2_v4"),
     ((2000, 64, 2048), "64x64x16_t8x8_s3_f2_v4"),
-    # 64 < N <= 128 with M >= 4096: the 128-wide tile, whatever K.
-    ((8192, 128, 1024), "256x128x64_t8x16_s2_f2_v4"),
-    ((8192, 96, 64), "256x128x64_t8x16_s2_f2_v4"),
+    # 64 < N <= 128 with M >= 4096: the 128-wide tile, 64-deep from 4 of its 64-deep
+    # slices a CTA, 32-deep from 1.25, else 128 x 128 tiles.
+    ((8192, 128, 4096), "256x128x64_t8x16_s2_f2_v4"),   # 32 * 64 = 2048 slices
+    ((4096, 96, 2432), "256x128x64_t8x16_s2_f2_v4"),    # 16 * 38 = 608 = 4 * 152
+    ((4096, 96, 2368), "256x128x32_t8x16_s4_f2_v4"),    # 16 * 37 = 592
+    ((8192, 128, 1024), "256x128x32_t8x16_s4_f2_v4"),   # 32 * 16 = 512
+    ((4096, 128, 768), "256x128x32_t8x16_s4_f2_v4"),    # 16 * 12 = 192 >= 190
+    ((4096, 128, 704), "128x128x32_t8x8_s3_f2_v4"),     # 16 * 11 = 176
+    ((4096, 128, 512), "128x128x32_t8x8_s3_f2_v4"),
+    ((8192, 96, 64), "128x128x32_t8x8_s3_f2_v4"),
+    # N <= 256 that 64-wide tiles fit more closely than 128-wide ones, M >= 4096.
+    ((8192, 192, 4096), "512x64x32_t8x16_s2_f2_v4"),
+    ((8192, 160, 1024), "512x64x32_t8x16_s2_f2_v4"),
+    ((8192, 256, 4096), "256x128x64_t8x16_s2_f2_v4"),   # both fit: 2 x 128
+    ((4000, 192, 4096), "256x128x64_t8x16_s2_f2_v4_burst"),  # M below 4096: general rules
+    # Short, wide C (M <= 64): tiles no taller than C.
+    ((64, 8192, 4096), "64x64x16_t8x8_s3_f2_v4"),
+    ((48, 4096, 1024), "64x64x16_t8x8_s3_f2_v4"),
+    ((32, 16384, 4096), "32x32x16_t4x4_s3_f2_v4"),
+    ((96, 4096, 4096), "128x256x32_t8x16_s4_f2_v4"),    # M above 64: small-C rules
+    # Small C with N <= 128: the 256 x 128 orientation.
+    ((2048, 128, 2048), "256x128x32_t8x16_s4_f2_v4"),
     # Below M = 4096 that rule yields: 32 tiles of 128^2 are fewer than SMs/4.
     ((4095, 128, 1024), "64x64x16_t8x8_s3_f2_v4"),
     ((2048, 256, 1024), "64x64x16_t8x8_s3_f2_v4"),     # 32 tiles of 128^2
