@@ -680,10 +680,15 @@ int launch_transpose(const float* X, long long ldx, int rows, int cols, float* Y
     return SGEMM_OK;
 }
 
-// Large problems whose A or B rows are not 16-byte aligned are worth copying to
-// aligned buffers first: the 4-byte-load kernels run ~16 % slower than the
-// 16-byte / TMA ones, the copy costs 8 bytes of traffic per operand element.
-constexpr double kPackMinMacs = 2147483648.0;   // M * N * K
+// Problems whose A or B rows are not 16-byte aligned are worth copying to aligned
+// buffers first once K is not short: the 4-byte-load kernels then run 15-40 %
+// slower than the 16-byte ones (copy included, 1024^3 29.7 against 36.4 TFLOP/s,
+// 1536 x 1536 x 768 34.5 against 43.9, 768 x 768 x 3000 27.7 against 41.3), while
+// with K of a few hundred they run as fast and the copy is pure cost (2048 x 2048 x
+// 511: 33.9 against 32.5).  The copy moves 8 bytes per operand element and takes
+// two launches, so the product must be large enough to pay for them.
+constexpr double kPackMinMacs = 5.0e8;   // M * N * K
+constexpr int kPackMinK = 768;
 
 // Operand staging in the library workspace: a transposed operand is always
 // transposed into a row-major buffer; a misaligned one of a large problem is
@@ -704,7 +709,7 @@ PackPlan pack_plan(int M, int N, int K, const float* A, int lda, const float* B,
     q.trans_b = transb != 0;
     // Each non-transposed operand is packed on its own: a transposed partner is
     // staged aligned anyway, so the other one alone decides the load width.
-    const bool pack = library_ws && forced_entry < 0 &&
+    const bool pack = library_ws && forced_entry < 0 && K >= kPackMinK &&
                       static_cast<double>(M) * N * K >= kPackMinMacs;
     q.pack_a = q.trans_a || (pack && !(aligned16(A) && lda % 4 == 0));
     q.pack_b = q.trans_b || (pack && !(aligned16(B) && ldb % 4 == 0));

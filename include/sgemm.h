@@ -107,9 +107,9 @@ typedef struct {
  * resident wave of tiles may instead split every tile's K range over a
  * thread-block cluster of 2, 4 or 8 CTAs that sum their partial tiles in
  * distributed shared memory, in k order, inside the one launch; that needs no
- * workspace (sgemm_query_config reports it as `cluster`).  Large problems (M*N*K >=
- * 2^31) whose A or B rows are not 16-byte aligned are first copied row by row
- * into aligned buffers in that workspace (one more launch per copied operand),
+ * workspace (sgemm_query_config reports it as `cluster`).  Problems with K >= 768
+ * and M*N*K >= 5e8 whose A or B rows are not 16-byte aligned are first copied row
+ * by row into aligned buffers in that workspace (one more launch per copied operand),
  * so they run on the 16-byte / TMA kernels (the copy moves values, not sums: the
  * results are those of the aligned kernels on aligned operands; they can differ
  * from the 4-byte-load kernels' in rounding, as any two tilings can, and stay

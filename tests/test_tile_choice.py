@@ -117,19 +117,25 @@ def test_sm_count_moves_the_thresholds(lib):
 
 
 def test_misaligned_operands_small_products_take_scalar_loads(lib):
-    # Below 2^31 multiply-adds nothing is packed: 4-byte loads.
-    assert _choose(lib, 1000, 1000, 1000, lda=1001) == ("128x256x32_t8x16_s3_f2_v1", 0)
-    assert _choose(lib, 1000, 1000, 1000, b_off=2) == ("128x256x32_t8x16_s3_f2_v1", 0)
+    # Below 5e8 multiply-adds, or with K < 768, nothing is packed: 4-byte loads.
+    assert _choose(lib, 700, 700, 1000, lda=1001) == ("64x64x16_t8x8_s3_f2_v1", 0)   # 4.9e8
+    assert _choose(lib, 800, 800, 780, lda=781) == ("128x256x32_t8x16_s3_f2_v1", 0)  # 4.99e8
     assert _choose(lib, 300, 300, 300, ldb=301) == ("64x64x16_t8x8_s3_f2_v1", 0)
+    assert _choose(lib, 4096, 4096, 767, lda=769)[1] == 0     # K just short of 768
+    assert _choose(lib, 2048, 2048, 511, b_off=2)[1] == 0
     # The 16-byte-load-only rules do not apply without aligned operands.
     assert _choose(lib, 16384, 64, 100, lda=101) == ("128x256x32_t8x16_s3_f2_v1", 0)
 
 
 def test_misaligned_operands_large_products_are_packed(lib):
-    # 1291^3 >= 2^31: the misaligned operand alone is packed, then the aligned rules apply.
+    # K >= 768 and M*N*K >= 5e8: the misaligned operand alone is packed, then the
+    # aligned rules apply.
+    assert _choose(lib, 1000, 1000, 1000, lda=1001) == ("128x256x32_t8x16_s4_f2_v4", 1)
+    assert _choose(lib, 1000, 1000, 1000, b_off=2) == ("128x256x32_t8x16_s4_f2_v4", 2)
+    assert _choose(lib, 800, 800, 782, lda=783)[1] == 1     # 5.0e8
+    assert _choose(lib, 4096, 4096, 768, lda=769)[1] == 1
     assert _choose(lib, 1291, 1292, 1292, lda=1293) == ("128x256x32_t8x16_s4_f2_v4", 1)
     assert _choose(lib, 1292, 1292, 1292, b_off=1) == ("128x256x32_t8x16_s4_f2_v4", 2)
-    assert _choose(lib, 1290, 1292, 1288, lda=1289)[1] == 0     # 1290*1292*1288 < 2^31
     # The ragged workload: odd leading dimensions everywhere, both packed.
     assert _choose(lib, 3001, 2047, 1999, lda=2001, ldb=2049) == ("256x128x64_t8x16_s2_f2_v4_burst",
                                                                  3)
