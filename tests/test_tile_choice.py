@@ -118,8 +118,12 @@ def test_sm_count_moves_the_thresholds(lib):
 
 def test_misaligned_operands_small_products_take_scalar_loads(lib):
     # Below 5e8 multiply-adds, or with K < 768, nothing is packed: 4-byte loads.
-    assert _choose(lib, 700, 700, 1000, lda=1001) == ("64x64x16_t8x8_s3_f2_v1", 0)   # 4.9e8
-    assert _choose(lib, 800, 800, 780, lda=781) == ("128x256x32_t8x16_s3_f2_v1", 0)  # 4.99e8
+    assert _choose(lib, 700, 700, 1000, lda=1001) == ("128x128x16_t16x8_s4_f2_v1", 0)  # 4.9e8
+    assert _choose(lib, 1000, 1000, 300, lda=301) == ("128x128x16_t16x8_s4_f2_v1", 0)  # 64 tiles
+    assert _choose(lib, 1500, 1500, 700, lda=701) == ("128x256x32_t8x16_s3_f2_v1", 0)  # 144 tiles
+    assert _choose(lib, 512, 512, 512, lda=513) == ("64x64x16_t8x8_s3_f2_v1", 0)       # 16 tiles
+    assert _choose(lib, 4096, 64, 300, lda=301) == ("64x64x16_t8x8_s3_f2_v1", 0)      # N = 64
+    assert _choose(lib, 800, 800, 780, lda=781) == ("128x128x16_t16x8_s4_f2_v1", 0)  # 4.99e8
     assert _choose(lib, 300, 300, 300, ldb=301) == ("64x64x16_t8x8_s3_f2_v1", 0)
     assert _choose(lib, 4096, 4096, 767, lda=769)[1] == 0     # K just short of 768
     assert _choose(lib, 2048, 2048, 511, b_off=2)[1] == 0
