@@ -500,3 +500,35 @@ def test_large_unaligned_operands_are_packed(cuda, oracle_mod):
     check_canary(buf, M, N)
     ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
     assert np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref)) <= tolerance(A, B)
+
+
+@pytest.mark.parametrize("M,N,K,a_off,name,packed", [
+    (64, 8192, 1024, 0, "64x64x16_t8x8_s3_f2_v4", 0),        # short, wide C
+    (32, 4000, 1000, 0, "32x32x16_t4x4_s3_f2_v4", 0),
+    (8192, 192, 1000, 0, "512x64x32_t8x16_s2_f2_v4", 0),     # 64-wide tiles fit N
+    (4096, 128, 1024, 0, "256x128x32_t8x16_s4_f2_v4", 0),    # slices on offer
+    (4096, 128, 512, 0, "128x128x32_t8x8_s3_f2_v4", 0),
+    (448, 448, 4096, 0, "128x256x32_t8x16_s4_f2_v4", 0),     # small C, deep K
+    (384, 384, 2048, 0, "128x128x32_t8x8_s3_f2_v4", 0),
+    (2048, 128, 2048, 0, "256x128x32_t8x16_s4_f2_v4", 0),
+    (1000, 1000, 300, 1, "128x128x16_t16x8_s4_f2_v1", 0),    # 4-byte loads, mid band
+    (1000, 1000, 1000, 1, "128x256x32_t8x16_s4_f2_v4", 1),   # misaligned A copied
+])
+def test_rule_choices_through_the_automatic_path(cuda, oracle_mod, M, N, K, a_off, name,
+                                                  packed):
+    """Each tile-choice rule, taken by sgemm_run itself (no forced entry), against
+    the oracle; a_off = 1 shifts A by 4 bytes so its rows are not 16-byte aligned."""
+    torch = cuda
+    A, B = random_pair(M, N, K, seed=M + N + K)
+    buf = torch.empty(M * K + a_off, device="cuda")
+    dA = buf[a_off:].view(M, K)
+    dA.copy_(A)
+    dB = B.cuda()
+    cfg = sgemm_query_config(M, N, K, K, N, N, dA.data_ptr(), dB.data_ptr(), None)
+    assert (cfg["name"], cfg["packed"]) == (name, packed)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    sgemm(dA, dB, out=C)
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm_f64(A.numpy(), B.numpy())
+    err = float(np.max(np.abs(C.cpu().numpy().astype(np.float64) - ref)))
+    assert np.isfinite(err) and err <= tolerance(A, B), err
