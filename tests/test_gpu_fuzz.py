@@ -100,16 +100,20 @@ def test_random_tf32x3_cases(cuda, oracle_mod, seed):
 def wide_case(rng):
     """Large shapes drawn around the tile chooser's boundaries: narrow C with M >= 4096
     (512 x 64 tiles), 64 < N <= 128, K around 2048 (slice depth), the smallest problems
-    (32 x 32 tiles), long K, and short K.  Operands 16-byte aligned."""
-    kind = int(rng.integers(0, 6))
+    (32 x 32 tiles), long K, short K, short and wide C (M <= 64), N from 129 to 256 with
+    M >= 4096 (64-wide tiles), small C with deep K, and N <= 128 with short K.
+    Operands 16-byte aligned."""
+    kind = int(rng.integers(0, 10))
     lo_hi = [((4000, 4600), (1, 65), (1, 2500)), ((4000, 4600), (65, 129), (1, 1500)),
              ((1000, 2600), (1000, 2600), (900, 2100)), ((1, 400), (1, 400), (1, 1100)),
-             ((500, 1400), (500, 1400), (1, 4000)), ((1, 2500), (1, 2500), (1, 64))][kind]
+             ((500, 1400), (500, 1400), (1, 4000)), ((1, 2500), (1, 2500), (1, 64)),
+             ((1, 100), (2000, 9000), (1, 3000)), ((4000, 8300), (129, 257), (1, 2500)),
+             ((200, 900), (200, 900), (2000, 6000)), ((4000, 9000), (65, 129), (64, 1500))][kind]
     M, N, K = (int(rng.integers(a, b)) for a, b in lo_hi)
     return M, N, K
 
 
-@pytest.mark.parametrize("seed", range(60))
+@pytest.mark.parametrize("seed", range(100))
 def test_random_wide_cases(cuda, oracle_mod, monkeypatch, seed):
     """Wide random cases on 16-byte-aligned operands (the 16-byte entries), with random
     alpha/beta and stream-K gaps forced to 0..3 or left to the planner."""
@@ -140,6 +144,44 @@ def test_random_wide_cases(cuda, oracle_mod, monkeypatch, seed):
     tol = 1e-6 * (abs(alpha) * K + abs(beta)) + 1e-30
     assert err <= tol, ((M, N, K, alpha, beta, gap), err, tol)
     flat = cbuf.cpu().numpy()
+    mask = np.ones(flat.size, dtype=bool)
+    for r in range(M):
+        mask[r * ldc: r * ldc + N] = False
+    assert np.all(flat[mask] == CANARY)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_misaligned_cases_around_the_copy_threshold(cuda, oracle_mod, seed):
+    """Operands with 4-byte-misaligned bases or odd leading dimensions, with M, N and K
+    drawn around the point from which sgemm copies them to aligned buffers (K >= 768
+    and M*N*K >= 5e8): both the copied path and the 4-byte-load kernels, checked
+    element by element against the oracle inside canaried C."""
+    torch = cuda
+    rng = np.random.default_rng(5000 + seed)
+    M, N = (int(x) for x in rng.integers(500, 1300, size=2))
+    K = int(rng.integers(500, 1400))
+    alpha = float(rng.choice([1.0, -1.5]))
+    beta = float(rng.choice([0.0, 1.0]))
+    pads = [int(x) for x in rng.integers(0, 4, size=3)]
+    offs = [int(x) for x in rng.integers(0, 2, size=3)]
+    if not any(pads[:2]) and not any(offs[:2]):
+        offs[0] = 1                      # at least one operand misaligned
+    g = torch.Generator().manual_seed(5000 + seed)
+    A = torch.rand(M, K, generator=g) * 2 - 1
+    B = torch.rand(K, N, generator=g) * 2 - 1
+    C0 = torch.rand(M, N, generator=g) * 2 - 1
+    _, dA, lda = place(torch, A, pads[0], offs[0], float("nan"))
+    _, dB, ldb = place(torch, B, pads[1], offs[1], float("nan"))
+    cbuf, dC, ldc = place(torch, C0, pads[2], offs[2], CANARY)
+    st = sgemm_run_op(0, 0, M, N, K, alpha, dA.data_ptr(), lda, dB.data_ptr(), ldb, beta,
+                      dC.data_ptr(), ldc)
+    assert st == 0, (M, N, K, load().sgemm_last_error())
+    torch.cuda.synchronize()
+    ref = oracle_mod.gemm_f64_ex(alpha, A.numpy(), B.numpy(), beta, C0.numpy())
+    err = np.max(np.abs(dC.cpu().numpy().astype(np.float64) - ref))
+    tol = 1e-6 * (abs(alpha) * K + abs(beta)) + 1e-30
+    assert err <= tol, ((M, N, K, pads, offs), err, tol)
+    flat = cbuf.cpu().numpy()[offs[2]:]
     mask = np.ones(flat.size, dtype=bool)
     for r in range(M):
         mask[r * ldc: r * ldc + N] = False
