@@ -241,7 +241,9 @@ SGEMM_API int sgemm_run_op(int transa, int transb, int M, int N, int K, float al
  * k-chunks (beta = 1 after the first) as its chunk of A and B arrives, the other
  * panels start once their rows of A are in, and each finished panel is copied
  * back while the next one is computed.  Rounding can differ from sgemm_run's by
- * that chunking; the error bound is the same.  The call returns when the work is
+ * that chunking; the error bound is the same.  A problem planned as one panel
+ * (fewer than 5e8 multiply-adds) has nothing to overlap: its copies and product
+ * are queued on `stream` itself.  The call returns when the work is
  * queued; synchronise
  * `stream` before reading hC.  Calls from several host threads are serialised
  * while they queue.  Errors: as sgemm_run, plus SGEMM_ERR_INVALID_ARG for a null

@@ -396,12 +396,14 @@ def test_host_entry_row_panels(cuda, oracle_mod, monkeypatch, panels, M, N, K):
     assert np.all(got[:, N:] == SENTINEL)
 
 
-def test_host_entry_is_ordered_on_the_callers_stream(cuda, oracle_mod, monkeypatch):
+@pytest.mark.parametrize("panels", ["4", "1"])
+def test_host_entry_is_ordered_on_the_callers_stream(cuda, oracle_mod, monkeypatch, panels):
     """Work queued on the stream before the call finishes before the call's
-    copies and products start, and work queued after it sees the finished C."""
+    copies and products start, and work queued after it sees the finished C: with
+    4 panels on the library's own streams, and with 1 on the caller's stream."""
     torch = cuda
     from dense_fp32_gemm_09_gb300 import check, sgemm_run_host
-    monkeypatch.setenv("SGEMM_HOST_PANELS", "4")
+    monkeypatch.setenv("SGEMM_HOST_PANELS", panels)
     M, N, K = 1024, 512, 384
     A, B = random_pair(M, N, K, seed=12)
     hA, hB = A.pin_memory(), B.pin_memory()
