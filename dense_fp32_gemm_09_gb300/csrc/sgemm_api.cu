@@ -317,7 +317,9 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
     } else if (v4) {
         // 64-deep slices run about 3% faster; 32-deep ones share K out more finely
         // over the stream-K ranges.  The deeper ones win once every CTA gets about
-        // 20 of them (measured from 1536^3, where they lose, to 4096x4096x1536).
+        // 16 of them, whatever K (1536^3, 11 a CTA, loses; 2048^3, 27, wins; with
+        // K = 2048 but 5 a CTA, 896 x 768 x 2048 ran 35.9 TFLOP/s on 64-deep slices
+        // against 43.9 on 32-deep ones, 768 x 1024 x 2048 42.1 against 44.5).
         // Among the 64-deep entries the one with double-buffered fragments (128 x
         // 256) wins once every CTA gets about 44 of its slices (4096^3 65.9 against
         // 64.4 TFLOP/s, 8192^3 67.1 against 65.2, 3072^3 64.1 against 63.2,
@@ -336,7 +338,7 @@ int choose_by_rules(int sms, int M, int N, int K, bool v4) {
         const bool ragged_h = (M % 256 != 0 || N % 128 != 0) && 2 * tiles_h < 3LL * sms;
         if (per_cta64 >= 44 && !ragged_h)
             name = "128x256x64_t8x16_s2_f2_v4";
-        else if (K >= 2048 || slices64 >= 20LL * sms)
+        else if (slices64 >= 16LL * sms)
             name = ragged_h ? "256x128x64_t8x16_s2_f2_v4_burst" : "256x128x64_t8x16_s2_f2_v4";
         else
             name = "128x256x32_t8x16_s4_f2_v4";

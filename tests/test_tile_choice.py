@@ -31,8 +31,8 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     ((4096, 4096, 1536), "128x256x64_t8x16_s2_f2_v4"),  # 512 * 24 / 152 = 80
     ((8192, 8192, 512), "128x256x64_t8x16_s2_f2_v4"),   # 2048 * 8 / 152 = 107
     ((3072, 3072, 1536), "128x256x64_t8x16_s2_f2_v4"),  # 288 * 24 / 152 = 45
-    # ... else 64-deep slices on 256 x 128 tiles once K >= 2048 or every CTA gets
-    # about 20 of them ...
+    # ... else 64-deep slices on 256 x 128 tiles once every CTA gets about 16 of
+    # them (tiles of 256 x 128 times 64-deep slices a tile, over 152 SMs) ...
     ((2048, 2048, 2048), "256x128x64_t8x16_s2_f2_v4"),  # 128 * 32 / 152 = 26
     ((2560, 2560, 1280), "256x128x64_t8x16_s2_f2_v4"),  # 200 * 20 / 152 = 26
     ((4096, 4096, 768), "256x128x64_t8x16_s2_f2_v4"),   # 512 * 12 / 152 = 40
@@ -40,8 +40,10 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     # slices; 1536^3: 1728).
     ((1024, 1024, 1024), "128x256x32_t8x16_s4_f2_v4"),
     ((1536, 1536, 1536), "128x256x32_t8x16_s4_f2_v4"),
-    ((1024, 2048, 2044), "128x256x32_t8x16_s4_f2_v4"),  # 4*16*32 = 2048 < 20*152
-    ((1536, 2048, 2044), "256x128x64_t8x16_s2_f2_v4"),  # 6*16*32 = 3072 >= 20*152
+    ((1024, 2048, 2044), "128x256x32_t8x16_s4_f2_v4"),  # 4*16*32 = 2048 < 16*152
+    ((1536, 2048, 2044), "256x128x64_t8x16_s2_f2_v4"),  # 6*16*32 = 3072 >= 16*152
+    ((896, 768, 2048), "128x256x32_t8x16_s4_f2_v4"),    # K = 2048 but 4*6*32 = 768
+    ((768, 1024, 2048), "128x256x32_t8x16_s4_f2_v4"),   # 3*8*32 = 768
     # Tiles crossing M or N with under 1.5 waves of 256 x 128 tiles: the all-burst twin.
     ((3008, 2048, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # 12*16 = 192 < 228
     ((3500, 2048, 2048), "256x128x64_t8x16_s2_f2_v4_burst"),  # 14*16 = 224
@@ -88,7 +90,7 @@ def _choose(lib, M, N, K, lda=None, ldb=None, a_off=0, b_off=0, sms=GB300_SMS):
     ((8192, 192, 4096), "512x64x32_t8x16_s2_f2_v4"),
     ((8192, 160, 1024), "512x64x32_t8x16_s2_f2_v4"),
     ((8192, 256, 4096), "256x128x64_t8x16_s2_f2_v4"),   # both fit: 2 x 128
-    ((4000, 192, 4096), "256x128x64_t8x16_s2_f2_v4_burst"),  # M below 4096: general rules
+    ((4000, 192, 4096), "128x256x32_t8x16_s4_f2_v4"),   # M below 4096: general rules
     # Short, wide C (M <= 64): tiles no taller than C.
     ((64, 8192, 4096), "64x64x16_t8x8_s3_f2_v4"),
     ((48, 4096, 1024), "64x64x16_t8x8_s3_f2_v4"),
